@@ -1,0 +1,433 @@
+"""Pins for the float64 oracle: facts fixed by the pages and by mathematics,
+checked without the oracle checking itself.
+
+Each test states what pins what:
+
+* library routine: vanilla attention equals torch's scaled_dot_product_attention
+  run in float64 on the CPU (GQA by explicit head repetition);
+* special cases: one cached token returns that token's value row; a zero query
+  returns the mean of the value rows;
+* exact identities from the pages: Lite (K^n, V^1) is fused attention with
+  weights (0, 1, 1, 0) ([Slides] Eq.(6) vs Eqs.(4)-(5)); fused attention with
+  constant channel weights equals plain attention over the explicitly summed
+  caches;
+* closed form of [Slides] Eqs.(7)-(8): with pair-tied key weights, shifting every
+  position by the same amount leaves the scores unchanged; untied weights break
+  this, by an amount that vanishes as the pair weights are made equal;
+* linearity of Eq.(5) in the value weights;
+* brute-force scalar loops on tiny shapes;
+* Table 1 and the notes' element counts (golden fixtures under tests/golden/).
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+def _caches(rng, L, B, H_kv, S, D, layers=None):
+    layers = layers or range(1, L + 1)
+    k = {l: rng.standard_normal((B, H_kv, S, D)) for l in layers}
+    v = {l: rng.standard_normal((B, H_kv, S, D)) for l in layers}
+    return k, v
+
+
+def _weights(rng, H_kv, D, tie=True):
+    ws = []
+    for i in range(4):
+        x = rng.normal(0.5, 0.3, (H_kv, D))
+        if tie and i < 2:
+            x[:, D // 2:] = x[:, : D // 2]
+        ws.append(x)
+    return tuple(ws)
+
+
+def _sdpa(q, k, v, causal=False, lens=None):
+    """torch SDPA in float64; q [B,H_q,T,D], k/v [B,H_kv,S,D]."""
+    G = q.shape[1] // k.shape[1]
+    qt = torch.from_numpy(np.ascontiguousarray(q))
+    kt = torch.from_numpy(np.ascontiguousarray(k)).repeat_interleave(G, dim=1)
+    vt = torch.from_numpy(np.ascontiguousarray(v)).repeat_interleave(G, dim=1)
+    if lens is None:
+        return torch.nn.functional.scaled_dot_product_attention(
+            qt, kt, vt, is_causal=causal).numpy()
+    outs = []
+    for b, n in enumerate(lens):
+        outs.append(torch.nn.functional.scaled_dot_product_attention(
+            qt[b:b + 1], kt[b:b + 1, :, :n], vt[b:b + 1, :, :n]).numpy())
+    return np.concatenate(outs, 0)
+
+
+# --------------------------------------------------------------------------
+# layer partition / sources ([Notes] §2.1, [Slides] Eq.(6) with its 16-layer
+# example)
+# --------------------------------------------------------------------------
+
+def test_lite_sources_sixteen_layers_golden():
+    g = _golden("lite_sources_16_layers.json")
+    L = g["num_layers"]
+    assert O.num_storage_layers(L) == len(g["storage_layers"])
+    for l in range(1, L + 1):
+        assert O.is_storage_layer(l, L) == (l in g["storage_layers"])
+    for l in g["reconstruction_layers"]:
+        src = O.kv_sources(l, L, O.LITE)
+        assert src["k"] == [g["lite_key_source"]] and src["v"] == [g["lite_value_source"]]
+        f = O.kv_sources(l, L, O.FUSED)
+        assert f["k"] == g["fused_sources"] and f["v"] == g["fused_sources"]
+    for l in g["storage_layers"]:
+        for m in O.MODES:
+            assert O.kv_sources(l, L, m) == {"k": [l], "v": [l], "weighted": False}
+
+
+def test_partition_rejects_odd_and_out_of_range():
+    with pytest.raises(ValueError):
+        O.num_storage_layers(7)
+    with pytest.raises(ValueError):
+        O.is_storage_layer(0, 4)
+    with pytest.raises(ValueError):
+        O.is_storage_layer(5, 4)
+
+
+# --------------------------------------------------------------------------
+# softmax attention against a library routine and closed-form special cases
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_decode_attention_matches_torch_sdpa(G):
+    rng = _rng(1)
+    B, H_kv, S, D = 3, 2, 37, 16
+    q = rng.standard_normal((B, H_kv * G, D))
+    k = rng.standard_normal((B, H_kv, S, D))
+    v = rng.standard_normal((B, H_kv, S, D))
+    lens = [37, 1, 20]
+    got = O.decode_attention(q, k, v, lens)
+    ref = _sdpa(q[:, :, None, :], k, v, lens=lens)[:, :, 0, :]
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_decode_attention_custom_scale_matches_sdpa():
+    rng = _rng(2)
+    q = rng.standard_normal((1, 2, 8))
+    k = rng.standard_normal((1, 1, 9, 8))
+    v = rng.standard_normal((1, 1, 9, 8))
+    got = O.decode_attention(q, k, v, [9], scale=0.3)
+    qt = torch.from_numpy(q[:, :, None, :])
+    kt = torch.from_numpy(k).expand(1, 2, 9, 8)
+    vt = torch.from_numpy(v).expand(1, 2, 9, 8)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=0.3)
+    np.testing.assert_allclose(got, ref[:, :, 0].numpy(), atol=1e-12)
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_prefill_attention_matches_torch_causal_sdpa(G):
+    rng = _rng(3)
+    B, H_kv, S, D = 2, 2, 23, 8
+    q = rng.standard_normal((B, H_kv * G, S, D))
+    k = rng.standard_normal((B, H_kv, S, D))
+    v = rng.standard_normal((B, H_kv, S, D))
+    got = O.prefill_attention(q, k, v)
+    ref = _sdpa(q, k, v, causal=True)
+    np.testing.assert_allclose(got, ref, atol=1e-12)
+    rows = [0, 5, 22]
+    got_rows = O.prefill_attention(q, k, v, rows=rows)
+    np.testing.assert_allclose(got_rows, ref[:, :, rows], atol=1e-12)
+
+
+def test_single_token_returns_value_row():
+    rng = _rng(4)
+    q = rng.standard_normal((2, 4, 8))
+    k = rng.standard_normal((2, 2, 5, 8))
+    v = rng.standard_normal((2, 2, 5, 8))
+    out = O.decode_attention(q, k, v, [1, 1])
+    for b in range(2):
+        for h in range(4):
+            np.testing.assert_array_equal(out[b, h], v[b, h // 2, 0])
+
+
+def test_zero_query_returns_mean_value():
+    rng = _rng(5)
+    q = np.zeros((1, 2, 8))
+    k = rng.standard_normal((1, 1, 11, 8))
+    v = rng.standard_normal((1, 1, 11, 8))
+    out = O.decode_attention(q, k, v, [7])
+    np.testing.assert_allclose(out[0, 0], v[0, 0, :7].mean(0), atol=1e-14)
+    np.testing.assert_allclose(out[0, 1], v[0, 0, :7].mean(0), atol=1e-14)
+
+
+def test_prefill_first_row_is_first_value():
+    rng = _rng(6)
+    q = rng.standard_normal((1, 2, 4, 8))
+    k = rng.standard_normal((1, 1, 4, 8))
+    v = rng.standard_normal((1, 1, 4, 8))
+    out = O.prefill_attention(q, k, v)
+    np.testing.assert_array_equal(out[0, 0, 0], v[0, 0, 0])
+
+
+def test_decode_rejects_empty_and_overlong():
+    q = np.zeros((1, 1, 4))
+    k = np.zeros((1, 1, 3, 4))
+    with pytest.raises(ValueError):
+        O.decode_attention(q, k, k, [0])
+    with pytest.raises(ValueError):
+        O.decode_attention(q, k, k, [4])
+
+
+# --------------------------------------------------------------------------
+# reconstruction ([Slides] Eqs.(4)-(6))
+# --------------------------------------------------------------------------
+
+def test_lite_equals_fused_with_zero_one_weights():
+    rng = _rng(7)
+    L, B, H_kv, S, D = 4, 2, 2, 19, 8
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2])
+    q = rng.standard_normal((B, 2 * H_kv, D))
+    z, o = np.zeros((H_kv, D)), np.ones((H_kv, D))
+    lens = [19, 6]
+    for layer in (3, 4):
+        lite = O.decode_attn(q, layer, L, O.LITE, kc, vc, lens)
+        fused = O.decode_attn(q, layer, L, O.FUSED, kc, vc, lens, weights={layer: (z, o, o, z)})
+        np.testing.assert_array_equal(lite, fused)
+
+
+def test_fused_unit_weights_select_sources():
+    """(a1, an, b1, bn) = (1, 0, 0, 1) is attention over (K^1, V^n): pins which
+    weight goes with which source."""
+    rng = _rng(8)
+    L, B, H_kv, S, D = 6, 1, 2, 13, 8
+    n = 3
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2, 3])
+    q = rng.standard_normal((B, 2 * H_kv, D))
+    z, o = np.zeros((H_kv, D)), np.ones((H_kv, D))
+    got = O.decode_attn(q, 5, L, O.FUSED, kc, vc, [13], weights={5: (o, z, z, o)})
+    ref = _sdpa(q[:, :, None], kc[1], vc[n])[:, :, 0]
+    np.testing.assert_allclose(got, ref, atol=1e-12)
+
+
+def test_fused_constant_weights_match_sdpa_on_summed_caches():
+    rng = _rng(9)
+    L, B, H_kv, S, D = 4, 2, 2, 17, 8
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2])
+    q = rng.standard_normal((B, 4, D))
+    c = (0.7, -1.3, 2.1, -0.4)
+    ws = tuple(np.full((H_kv, D), x) for x in c)
+    got = O.decode_attn(q, 3, L, O.FUSED, kc, vc, [17, 17], weights={3: ws})
+    ref = _sdpa(q[:, :, None], c[0] * kc[1] + c[1] * kc[2], c[2] * vc[1] + c[3] * vc[2])[:, :, 0]
+    np.testing.assert_allclose(got, ref, atol=1e-12)
+
+
+def test_fused_per_head_channel_weights_match_sdpa():
+    """Channel weights differ per (head, channel) and are broadcast over batch
+    and tokens ([Slides] 'learned vectors broadcast over tokens')."""
+    rng = _rng(10)
+    L, B, H_kv, S, D = 4, 2, 2, 9, 6
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2])
+    q = rng.standard_normal((B, 4, D))
+    ws = _weights(rng, H_kv, D, tie=False)
+    got = O.decode_attn(q, 4, L, O.FUSED, kc, vc, [9, 9], weights={4: ws})
+    k_i = np.empty_like(kc[1])
+    v_i = np.empty_like(vc[1])
+    for b in range(B):
+        for h in range(H_kv):
+            for t in range(S):
+                k_i[b, h, t] = ws[0][h] * kc[1][b, h, t] + ws[1][h] * kc[2][b, h, t]
+                v_i[b, h, t] = ws[2][h] * vc[1][b, h, t] + ws[3][h] * vc[2][b, h, t]
+    np.testing.assert_allclose(got, _sdpa(q[:, :, None], k_i, v_i)[:, :, 0], atol=1e-12)
+
+
+def test_value_weights_act_linearly():
+    """For fixed scores, o(b1 V1 + bn Vn) = b1 o(V1) + bn o(Vn) (Eq.(5) is linear)."""
+    rng = _rng(11)
+    L, B, H_kv, S, D = 4, 1, 1, 15, 8
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2])
+    q = rng.standard_normal((B, 2, D))
+    a1, an, b1, bn = _weights(rng, H_kv, D)
+    z = np.zeros_like(b1)
+    full = O.decode_attn(q, 3, L, O.FUSED, kc, vc, [15], weights={3: (a1, an, b1, bn)})
+    only1 = O.decode_attn(q, 3, L, O.FUSED, kc, vc, [15], weights={3: (a1, an, np.ones_like(b1), z)})
+    onlyn = O.decode_attn(q, 3, L, O.FUSED, kc, vc, [15], weights={3: (a1, an, z, np.ones_like(bn))})
+    np.testing.assert_allclose(full, b1[0] * only1 + bn[0] * onlyn, atol=1e-12)
+
+
+def test_negative_and_unnormalised_weights_accepted():
+    rng = _rng(12)
+    L = 4
+    kc, vc = _caches(rng, L, 1, 1, 5, 4, layers=[1, 2])
+    q = rng.standard_normal((1, 1, 4))
+    ws = tuple(np.full((1, 4), x) for x in (-3.0, 5.0, -2.0, 7.5))
+    out = O.decode_attn(q, 3, L, O.FUSED, kc, vc, [5], weights={3: ws})
+    assert np.all(np.isfinite(out))
+
+
+@pytest.mark.parametrize("mode", O.MODES)
+@pytest.mark.parametrize("layer", [1, 2, 3, 4])
+def test_brute_force_matches_vectorised_decode(mode, layer):
+    rng = _rng(13)
+    L, B, H_kv, S, D = 4, 2, 2, 7, 4
+    kc, vc = _caches(rng, L, B, H_kv, S, D)
+    q = rng.standard_normal((B, 4, D))
+    ws = {l: _weights(rng, H_kv, D, tie=False) for l in (3, 4)}
+    lens = [7, 3]
+    a = O.decode_attn(q, layer, L, mode, kc, vc, lens, weights=ws)
+    b = O.brute_force_decode(q, layer, L, mode, kc, vc, lens, weights=ws)
+    np.testing.assert_allclose(a, b, atol=1e-12)
+
+
+def test_brute_force_matches_vectorised_prefill():
+    rng = _rng(14)
+    q = rng.standard_normal((1, 4, 6, 4))
+    k = rng.standard_normal((1, 2, 6, 4))
+    v = rng.standard_normal((1, 2, 6, 4))
+    np.testing.assert_allclose(O.prefill_attention(q, k, v), O.brute_force_prefill(q, k, v),
+                               atol=1e-12)
+
+
+def test_prefill_fused_uses_first_S_positions():
+    rng = _rng(15)
+    L, B, H_kv, Smax, S, D = 4, 1, 1, 12, 8, 4
+    kc, vc = _caches(rng, L, B, H_kv, Smax, D, layers=[1, 2])
+    q = rng.standard_normal((B, 2, S, D))
+    ws = {3: _weights(rng, H_kv, D)}
+    got = O.prefill_attn(q, 3, L, O.FUSED, kc, vc, weights=ws)
+    a1, an, b1, bn = ws[3]
+    k_i = a1[None, :, None] * kc[1][:, :, :S] + an[None, :, None] * kc[2][:, :, :S]
+    v_i = b1[None, :, None] * vc[1][:, :, :S] + bn[None, :, None] * vc[2][:, :, :S]
+    np.testing.assert_allclose(got, _sdpa(q, k_i, v_i, causal=True), atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# RoPE pair tying ([Slides] "Post-RoPE fusion needs paired key weights",
+# Eqs.(7)-(8); [Notes] §2.4)
+# --------------------------------------------------------------------------
+
+def test_rope_is_a_rotation_with_relative_composition():
+    rng = _rng(16)
+    D = 16
+    x = rng.standard_normal((5, D))
+    y = rng.standard_normal((5, D))
+    pos_x = np.array([0, 3, 10, 100, 7])
+    pos_y = np.array([2, 3, 0, 50, 1000])
+    rx, ry = O.rope_rotate_half(x, pos_x), O.rope_rotate_half(y, pos_y)
+    # position 0 is the identity; norms are kept
+    np.testing.assert_allclose(rx[0], x[0], atol=0)
+    np.testing.assert_allclose(np.linalg.norm(rx, axis=1), np.linalg.norm(x, axis=1), atol=1e-12)
+    # <R_m x, R_t y> = <x, R_{t-m} y>
+    lhs = np.sum(rx * ry, axis=1)
+    rhs = np.array([x[i] @ O.rope_rotate_half(y[i:i + 1], np.array([pos_y[i] - pos_x[i]]))[0]
+                    for i in range(5)])
+    np.testing.assert_allclose(lhs, rhs, atol=1e-10)
+    # rotate-half pairs channel j with j + D/2: a rotation by pi/2 of pair 0
+    e = np.zeros((1, D))
+    e[0, 0] = 1.0
+    th0 = O.rope_angles(np.array([1.0]), D)[0, 0]
+    r = O.rope_rotate_half(e, np.array([1.0]))[0]
+    assert r[0] == pytest.approx(math.cos(th0)) and r[D // 2] == pytest.approx(math.sin(th0))
+    assert np.count_nonzero(np.abs(r) > 1e-15) == 2
+
+
+def _scores_at_offset(q, k1, kn, a1, an, c):
+    T = k1.shape[0]
+    m = T - 1 + c
+    return O.fused_key_scores(q, m, k1, kn, np.arange(T) + c, a1, an)
+
+
+def test_tied_weights_make_scores_shift_invariant():
+    rng = _rng(17)
+    D, T = 32, 20
+    q = rng.standard_normal(D)
+    k1 = rng.standard_normal((T, D))
+    kn = rng.standard_normal((T, D))
+    a1, an, _, _ = (w[0] for w in _weights(rng, 1, D, tie=True))
+    assert O.tied(a1) and O.tied(an)
+    s0 = _scores_at_offset(q, k1, kn, a1, an, 0)
+    for c in (1, 17, 4096):
+        np.testing.assert_allclose(_scores_at_offset(q, k1, kn, a1, an, c), s0, atol=1e-10)
+
+
+def test_untied_weights_break_shift_invariance_in_proportion():
+    rng = _rng(18)
+    D, T = 32, 20
+    q = rng.standard_normal(D)
+    k1 = rng.standard_normal((T, D))
+    kn = rng.standard_normal((T, D))
+    a1, an, _, _ = (w[0] for w in _weights(rng, 1, D, tie=True))
+    delta = rng.standard_normal(D // 2)
+    diffs = []
+    for eps in (1.0, 0.1, 0.01):
+        u = a1.copy()
+        u[D // 2:] += eps * delta  # untie: w_j != w_{j+D/2}
+        assert not O.tied(u)
+        d = np.max(np.abs(_scores_at_offset(q, k1, kn, u, an, 37)
+                          - _scores_at_offset(q, k1, kn, u, an, 0)))
+        diffs.append(d)
+    assert diffs[0] > 1e-3
+    # the absolute-position term is proportional to (w_j - w_{j+D/2})
+    assert diffs[1] == pytest.approx(diffs[0] * 0.1, rel=1e-6)
+    assert diffs[2] == pytest.approx(diffs[0] * 0.01, rel=1e-6)
+
+
+# --------------------------------------------------------------------------
+# cache capacity / I/O ([Slides] Table 1; [Notes] §2.5 element counts)
+# --------------------------------------------------------------------------
+
+def test_table1_capacity_and_io_ratios():
+    g = _golden("table1_capacity_io.json")
+    L, S, H, D = 16, 1000, 4, 64
+    LSHD = L * S * H * D
+    for m in O.MODES:
+        assert O.stored_elements(m, L, S, H, D) / O.stored_elements(O.VANILLA, L, S, H, D) \
+            == g["capacity"][m]
+        assert O.step_read_elements(m, L, S, H, D) / O.step_read_elements(O.VANILLA, L, S, H, D) \
+            == g["io"][m]
+        assert O.step_read_elements(m, L, S, H, D) == g["elements_in_units_of_LSHD"][m + "_step"] * LSHD
+    lower = sum(O.call_read_elements(l, O.FUSED, L, S, H, D) for l in range(1, L // 2 + 1))
+    upper = sum(O.call_read_elements(l, O.FUSED, L, S, H, D) for l in range(L // 2 + 1, L + 1))
+    assert lower == g["elements_in_units_of_LSHD"]["fused_lower_half"] * LSHD
+    assert upper == g["elements_in_units_of_LSHD"]["fused_upper_half"] * LSHD
+    # the plain element count of the pages: 2 L S H_kv D
+    assert O.stored_elements(O.VANILLA, L, S, H, D) == 2 * LSHD
+
+
+def test_gqa_composition_golden():
+    g = _golden("composed_capacity.json")
+    L, S, D, H_q = 8, 64, 16, 8
+    mha = O.stored_elements(O.VANILLA, L, S, H_q, D)
+    gqa = O.stored_elements(O.VANILLA, L, S, H_q // g["gqa_group"], D)
+    fkv = O.stored_elements(O.FUSED, L, S, H_q // g["gqa_group"], D)
+    assert gqa / mha == g["gqa_vs_mha"]
+    assert fkv / mha == g["gqa_fusedkv_vs_mha"]
+    # 4-bit payload on top of FusedKV, against fp16 vanilla with the same heads
+    van = O.stored_elements(O.VANILLA, L, S, H_q // g["gqa_group"], D)
+    assert (fkv * 4) / (van * 16) == g["fusedkv_4bit_vs_fp16_vanilla"]
+
+
+# --------------------------------------------------------------------------
+# append ([Notes] §2.3: new tokens enter the storage caches first)
+# --------------------------------------------------------------------------
+
+def test_append_writes_rows_at_offsets_only():
+    rng = _rng(19)
+    cache = rng.standard_normal((2, 2, 10, 4))
+    new = rng.standard_normal((2, 2, 3, 4))
+    out = O.append_kv(cache, new, [0, 7])
+    np.testing.assert_array_equal(out[0, :, 0:3], new[0])
+    np.testing.assert_array_equal(out[1, :, 7:10], new[1])
+    np.testing.assert_array_equal(out[0, :, 3:], cache[0, :, 3:])
+    np.testing.assert_array_equal(out[1, :, :7], cache[1, :, :7])
+    with pytest.raises(ValueError):
+        O.append_kv(cache, new, [8, 0])
