@@ -1,0 +1,510 @@
+#!/usr/bin/env python
+"""Benchmark of the FusedKV decode hot path on GB300.
+
+A step is one attention-only decode step of the 332M-shaped model (12 layers,
+storage layers 1-6, 16 Q / 8 KV heads, D=64, bf16 caches, batch 32, 8192
+cached tokens per sequence), as the FusedKV Table 1 accounting counts it:
+  * fkv_append_kv of the new token's K/V into every layer that stores
+    (layers 1-6; all 12 in vanilla mode), then
+  * fkv_decode_attn for layers 1..12 in order (upper layers in the mode under
+    test: vanilla reads their own cache, lite K^6/V^1, fused K^1,K^6,V^1,V^6).
+`value` is fused-mode decode tokens/s (batch / step time) with every input
+resident in HBM; `modes` holds all three modes; `e2e` repeats the fused step
+through the same C-ABI calls with the per-step inputs copied from pinned host
+memory and the outputs read back inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 (torchrun) every rank runs an independent replica (the path shards
+by sequence with no exchange), rank 0 prints the max-over-ranks timing.
+"""
+
+from __future__ import annotations
+
+import os
+
+# The oracle baseline runs single-threaded so that `cores` is exact.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("decode tokens/s & KV GB/s (% of 8 TB/s HBM) for fused/lite/vanilla; "
+          "prefill TFLOP/s")
+HBM_REF_GBS = 8000.0
+
+# DRAM traffic (read + write bytes per launch) of the fused split kernel on
+# this workload, from one ncu capture, and the source hash of the kernel it was
+# taken on; reported only while the kernel is unchanged.
+NCU_TRAFFIC = {"bytes_per_launch": None, "kernel_sha": None,
+               "profile": "profiles/decode_split_fused_332M.md"}
+
+
+def _kernel_sha():
+    h = hashlib.sha256()
+    for f in ("decode_impl.cuh", "fkv_device.cuh"):
+        with open(os.path.join(ROOT, "cross_layer_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the decode model (caches for all 12 layers so vanilla can run)
+# ---------------------------------------------------------------------------
+
+class DecodeModel:
+    def __init__(self, w, device, seed=0):
+        import cross_layer_kv_gb300 as fkv
+        from cross_layer_kv_gb300 import synth
+        self.w = w
+        self.dev = device
+        L, n = w.num_layers, w.n
+        self.ctx = fkv.Context(L, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim, w.dtype,
+                               store_upper=True)
+        self.caches = {}
+        for l in range(1, L + 1):
+            k, v = synth.make_cache(w, l, seed, device)
+            self.caches[l] = (k, v)
+            self.ctx.fkv_bind_layer_cache(l, k, v)
+        self.weights = {}
+        for l in range(n + 1, L + 1):
+            self.weights[l] = synth.make_weights(w, l, seed, device)
+            self.ctx.fkv_set_fusion_weights(l, *self.weights[l])
+        # per-step inputs: queries of every layer, the new token's K/V per layer
+        self.q = torch.stack([synth.make_query(w, l, seed + 1, device) for l in range(1, L + 1)])
+        g = torch.Generator(device=device).manual_seed(seed + 2)
+        shape = (L, w.batch, w.kv_heads, 1, w.head_dim)
+        self.k_new = torch.randn(shape, generator=g, device=device).to(w.torch_dtype)
+        self.v_new = torch.randn(shape, generator=g, device=device).to(w.torch_dtype)
+        # every sequence is full: the new token is written at row S-1 and all
+        # S rows are attended (the step shape stays fixed from step to step)
+        self.pos = torch.full((w.batch,), w.seq - 1, dtype=torch.int32, device=device)
+        self.lens = torch.full((w.batch,), w.seq, dtype=torch.int32, device=device)
+        self.out = torch.empty_like(self.q)
+        self.ws = self.ctx.workspace(device)
+
+    def appended_layers(self, mode):
+        return range(1, self.w.num_layers + 1) if mode == "vanilla" else range(1, self.w.n + 1)
+
+    def launches_per_step(self, mode):
+        from cross_layer_kv_gb300.fusedkv import DECODE_LAUNCHES_PER_CALL
+        return len(self.appended_layers(mode)) + DECODE_LAUNCHES_PER_CALL * self.w.num_layers
+
+    def step(self, mode, stream, upper_events=None):
+        c = self.ctx
+        for l in self.appended_layers(mode):
+            c.fkv_append_kv(l, self.k_new[l - 1], self.v_new[l - 1], self.pos, 1, stream)
+        for l in range(1, self.w.num_layers + 1):
+            ev = upper_events is not None and l > self.w.n
+            if ev:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            c.fkv_decode_attn(self.q[l - 1], l, mode, self.lens, self.out[l - 1], self.ws, stream)
+            if ev:
+                e1.record(stream)
+                upper_events.append((e0, e1))
+
+    def call_bytes(self, layer, mode):
+        """Algorithmic cache bytes one decode call reads (K and V sources)."""
+        w = self.w
+        nsrc = 2 if (layer > w.n and mode == "fused") else 1
+        return 2 * nsrc * w.batch * w.kv_heads * w.seq * w.head_dim * w.elem_bytes
+
+    def step_bytes(self, mode):
+        return sum(self.call_bytes(l, mode) for l in range(1, self.w.num_layers + 1))
+
+    def close(self):
+        self.ctx.close()
+
+
+def _barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x, dist_on, device):
+    if not dist_on:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(model, mode, K, W, stream, dist_on, device, collect_upper=False):
+    for _ in range(W):
+        model.step(mode, stream)
+    torch.cuda.synchronize()
+    _barrier(dist_on)
+    torch.cuda.synchronize()
+    upper = [] if collect_upper else None
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        model.step(mode, stream, upper)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(dist_on)
+    ms = _max_over_ranks(e0.elapsed_time(e1), dist_on, device)
+    upper_ms = None
+    if upper:
+        upper_ms = statistics.fmean(a.elapsed_time(b) for a, b in upper)
+    return ms, upper_ms
+
+
+def time_e2e(model, K, W, stream, dist_on, device):
+    """Fused step through the C ABI with per-step inputs from pinned host
+    memory and the step's outputs read back, all inside the timed region."""
+    q_h = model.q.cpu().pin_memory()
+    kn_h = model.k_new.cpu().pin_memory()
+    vn_h = model.v_new.cpu().pin_memory()
+    out_h = torch.empty(model.out.shape, dtype=model.out.dtype).pin_memory()
+    n = model.w.n
+
+    def one():
+        with torch.cuda.stream(stream):
+            model.q.copy_(q_h, non_blocking=True)
+            model.k_new[:n].copy_(kn_h[:n], non_blocking=True)
+            model.v_new[:n].copy_(vn_h[:n], non_blocking=True)
+            model.step("fused", stream)
+            out_h.copy_(model.out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(W):
+        one()
+    torch.cuda.synchronize()
+    _barrier(dist_on)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        one()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    _barrier(dist_on)
+    dt = _max_over_ranks(dt, dist_on, device)
+    h2d = q_h.numel() * q_h.element_size() + 2 * kn_h[:n].numel() * kn_h.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+    return dt, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_decode_step_seconds(w, budget_s=12.0, seed=0):
+    """Time the float64 oracle on the attention-only fused decode step of
+    whole sequences (all 12 layers, one sequence at a time), as many
+    sequences as fit in about `budget_s` seconds.  Returns (s/token, sample)."""
+    import oracle as O
+    from cross_layer_kv_gb300 import synth
+    L, n = w.num_layers, w.n
+    one = synth.Workload(w.name, L, 1, w.seq, w.q_heads, w.kv_heads, w.head_dim, w.dtype)
+    caches, weights, qs = {}, {}, {}
+    for l in range(1, n + 1):
+        k, v = synth.make_cache(one, l, seed, "cpu")
+        caches[l] = (k.double().numpy(), v.double().numpy())
+    for l in range(n + 1, L + 1):
+        weights[l] = tuple(x.double().numpy() for x in synth.make_weights(one, l, seed, "cpu"))
+    for l in range(1, L + 1):
+        qs[l] = synth.make_query(one, l, seed, "cpu").double().numpy()
+    kc = {l: c[0] for l, c in caches.items()}
+    vc = {l: c[1] for l, c in caches.items()}
+    seqs = 0
+    t0 = time.perf_counter()
+    while True:
+        for l in range(1, L + 1):
+            O.decode_attn(qs[l], l, L, O.FUSED, kc, vc, [w.seq], weights=weights)
+        seqs += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or seqs >= 64:
+            break
+    return el / seqs, "%d whole sequence(s) x %d layers, fused mode, S=%d, 1 thread" % (
+        seqs, L, w.seq)
+
+
+def run_reference(args, rank, dist_on):
+    from cross_layer_kv_gb300 import synth
+    w = synth.M332
+    if rank != 0:
+        return
+    per_tok = []
+    sample = ""
+    for _ in range(args.warmup):
+        oracle_decode_step_seconds(w, budget_s=0.0)
+    for _ in range(args.steps):
+        s, sample = oracle_decode_step_seconds(w, budget_s=args.ref_budget)
+        per_tok.append(s)
+    sec = statistics.fmean(per_tok)
+    val = 1.0 / sec
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3 * w.batch, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "global_batch": w.batch * args.gpus,
+                       "seq_len": w.seq, "parallelism": "replicas"},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-budget", type=float, default=4.0)
+    ap.add_argument("--no-prefill", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    if args.impl == "reference":
+        if dist_on:
+            torch.distributed.init_process_group("gloo")
+        run_reference(args, rank, dist_on)
+        if dist_on:
+            torch.distributed.destroy_process_group()
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if dist_on:
+        torch.distributed.init_process_group("nccl", device_id=device)
+
+    from cross_layer_kv_gb300 import synth
+    import cross_layer_kv_gb300 as fkv
+    fkv.load()
+    w = synth.M332
+    model = DecodeModel(w, device)
+    stream = torch.cuda.Stream(device)
+    peaks = _peaks()
+    K, W = args.steps, args.warmup
+
+    modes = {}
+    clocks = None
+    upper_ms = None
+    launches = 0
+    for mode in ("vanilla", "lite", "fused"):
+        if mode == "fused":
+            with ClockSampler(local) as cs:
+                ms, upper_ms = time_steps(model, mode, K, W, stream, dist_on, device,
+                                          collect_upper=True)
+            clocks = cs.summary()
+            launches = K * model.launches_per_step(mode)
+        else:
+            ms, _ = time_steps(model, mode, K, W, stream, dist_on, device)
+        step_ms = ms / K
+        gb = model.step_bytes(mode) / 1e9
+        modes[mode] = {
+            "tokens_per_s": w.batch * world / (step_ms / 1e3),
+            "step_ms": step_ms,
+            "step_bytes_GB": gb,
+            "GBps": gb / (step_ms / 1e3),
+            "pct_of_8TBps": 100.0 * gb / (step_ms / 1e3) / HBM_REF_GBS,
+            "pct_of_measured_hbm": 100.0 * gb / (step_ms / 1e3) / peaks["hbm_gbs"],
+        }
+
+    # dominant kernel: the fused upper-layer decode call
+    call_bytes = model.call_bytes(w.num_layers, "fused")
+    achieved = call_bytes / (upper_ms / 1e3) / 1e9
+    traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["kernel_sha"] == _kernel_sha() else None
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "kernel": "fused upper-layer fkv_decode_attn (split + merge)",
+                "algorithmic_bytes_per_launch": call_bytes, "avg_launch_us": upper_ms * 1e3,
+                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)"}
+
+    e2e_s, h2d, d2h = time_e2e(model, max(20, K // 5), W, stream, dist_on, device)
+    e2e_steps = max(20, K // 5)
+    e2e = {"value": w.batch * world * e2e_steps / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "note": "fused step via the C ABI; per-step q and new K/V from pinned host memory, "
+                   "all 12 layer outputs read back, host sync every step"}
+
+    prefill = None
+    if not args.no_prefill:
+        prefill = bench_prefill(device, stream, peaks, W)
+
+    model.close()
+    del model
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        sec, sample = oracle_decode_step_seconds(w, budget_s=args.cpu_budget)
+        cpu = {"value": 1.0 / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": sample}
+
+    fused = modes["fused"]
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": fused["tokens_per_s"],
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": fused["step_ms"],
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name + " (12 layers, storage 1-6, B=32, S=8192, 16/8 heads, "
+                                   "D=64, bf16), attention-only decode step, fused mode",
+                       "global_batch": w.batch * world, "seq_len": w.seq,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (every call reads >= 0.5 GB)"},
+            "modes": modes,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if prefill is not None:
+            line["prefill"] = prefill
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+def bench_prefill(device, stream, peaks, W):
+    """Causal prefill of the 650M-shaped workload (B=4, S=8192, 16/8 heads,
+    D=96), one upper-layer call per mode; TFLOP/s counts unmasked work."""
+    import cross_layer_kv_gb300 as fkv
+    from cross_layer_kv_gb300 import synth
+    w = synth.M650_PREFILL
+    ctx = fkv.Context(w.num_layers, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim, "bf16",
+                      store_upper=True)
+    layer = w.num_layers
+    keep = []
+    for l in sorted({1, w.n, layer}):
+        k, v = synth.make_cache(w, l, 0, device)
+        keep.append((k, v))
+        ctx.fkv_bind_layer_cache(l, k, v)
+    wts = synth.make_weights(w, layer, 0, device)
+    ctx.fkv_set_fusion_weights(layer, *wts)
+    q = synth.make_query(w, layer, 0, device, positions=w.seq)
+    out = torch.empty_like(q)
+    flops = 4.0 * w.batch * w.q_heads * w.head_dim * w.seq * (w.seq + 1) / 2
+    res = {"workload": w.name + " (B=4, S=8192, 16/8 heads, D=96, bf16, causal)"}
+    try:
+        for mode in ("vanilla", "lite", "fused"):
+            for _ in range(W):
+                ctx.fkv_prefill_attn(q, layer, mode, w.seq, out, stream)
+            torch.cuda.synchronize()
+            reps = 10
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                ctx.fkv_prefill_attn(q, layer, mode, w.seq, out, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            tf = flops / (ms / 1e3) / 1e12
+            res[mode] = {"ms": ms, "TFLOPs": tf,
+                         "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+                         "peak": peaks["bf16_tflops"], "peak_source": peaks["source"] + " burst"}
+    except fkv.FkvError as e:
+        res["unavailable"] = str(e)
+    ctx.close()
+    return res
+
+
+if __name__ == "__main__":
+    main()

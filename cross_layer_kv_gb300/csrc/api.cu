@@ -1,0 +1,276 @@
+// The C ABI of include/fusedkv.h: context, host-side validation and dispatch
+// to the kernels.  Every check runs before any launch; nothing here allocates
+// on the hot path.
+#include <cmath>
+#include <cstdint>
+#include <new>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fusedkv.h"
+#include "fkv_kernels.h"
+
+struct fkv_ctx {
+  fkv_config cfg;
+  int n;          // storage layers 1..n
+  int group;      // H_q / H_kv
+  float scale;    // softmax scale
+  int device;
+  int num_sms;
+  int* status;    // device status word
+  std::vector<void*> k, v;                 // index: layer (1-based)
+  std::vector<const float*> w[4];          // a_first, a_second, b_first, b_second
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(const fkv_config& c) { return c.dtype == FKV_F32 ? 4 : 2; }
+
+fkv_status check_config(const fkv_config* c) {
+  if (!c) return FKV_ERR_INVALID_ARG;
+  if (c->num_layers < 2 || c->num_layers % 2) return FKV_ERR_INVALID_ARG;
+  if (c->batch < 1 || c->batch > 1024) return FKV_ERR_INVALID_ARG;
+  if (c->max_seq < 1) return FKV_ERR_INVALID_ARG;
+  if (c->num_kv_heads < 1 || c->num_q_heads < 1) return FKV_ERR_INVALID_ARG;
+  if (c->num_q_heads % c->num_kv_heads) return FKV_ERR_INVALID_ARG;
+  if (c->dtype != FKV_BF16 && c->dtype != FKV_F32) return FKV_ERR_INVALID_ARG;
+  if (!(c->softmax_scale >= 0.f) || !std::isfinite(c->softmax_scale)) return FKV_ERR_INVALID_ARG;
+  if (c->decode_ctas < 0 || c->decode_ctas > 65535) return FKV_ERR_INVALID_ARG;
+  if ((long long)c->batch * c->num_kv_heads * c->max_seq >= (1LL << 31)) return FKV_ERR_INVALID_ARG;
+  const int g = c->num_q_heads / c->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4) return FKV_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 80 && c->head_dim != 96 && c->head_dim != 128)
+    return FKV_ERR_UNSUPPORTED;
+  return FKV_OK;
+}
+
+// Resolve the cache / weight sources of a call.  nsrc = 1 or 2.
+fkv_status resolve_sources(const fkv_ctx* c, int layer, int mode, const void* k[2],
+                           const void* v[2], const float* a[2], const float* b[2], int* nsrc) {
+  if (layer < 1 || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
+  if (mode != FKV_VANILLA && mode != FKV_LITE && mode != FKV_FUSED) return FKV_ERR_INVALID_ARG;
+  k[0] = k[1] = v[0] = v[1] = nullptr;
+  a[0] = a[1] = b[0] = b[1] = nullptr;
+  const int n = c->n;
+  if (layer <= n || mode == FKV_VANILLA) {
+    if (layer > n && !c->cfg.store_upper) return FKV_ERR_UNSUPPORTED;
+    k[0] = c->k[layer];
+    v[0] = c->v[layer];
+    *nsrc = 1;
+    if (!k[0] || !v[0]) return FKV_ERR_INVALID_ARG;
+    return FKV_OK;
+  }
+  if (mode == FKV_LITE) {  // K^i = K^n, V^i = V^1
+    k[0] = c->k[n];
+    v[0] = c->v[1];
+    *nsrc = 1;
+    if (!k[0] || !v[0]) return FKV_ERR_INVALID_ARG;
+    return FKV_OK;
+  }
+  // fused: K^1, K^n with a_first, a_second; V^1, V^n with b_first, b_second
+  k[0] = c->k[1];
+  k[1] = c->k[n];
+  v[0] = c->v[1];
+  v[1] = c->v[n];
+  for (int i = 0; i < 2; ++i) {
+    a[i] = c->w[i][layer];
+    b[i] = c->w[2 + i][layer];
+  }
+  *nsrc = 2;
+  if (!k[0] || !k[1] || !v[0] || !v[1] || !a[0] || !a[1] || !b[0] || !b[1])
+    return FKV_ERR_INVALID_ARG;
+  return FKV_OK;
+}
+
+fkv::DecodeArgs decode_args(const fkv_ctx* c) {
+  fkv::DecodeArgs d{};
+  d.batch = c->cfg.batch;
+  d.kv_heads = c->cfg.num_kv_heads;
+  d.group = c->group;
+  d.max_seq = c->cfg.max_seq;
+  d.head_dim = c->cfg.head_dim;
+  d.is_f32 = c->cfg.dtype == FKV_F32;
+  d.softmax_scale = c->scale;
+  d.status = c->status;
+  d.num_ctas = c->cfg.decode_ctas;
+  return d;
+}
+
+}  // namespace
+
+extern "C" {
+
+fkv_status fkv_create(const fkv_config* cfg, fkv_ctx** out) {
+  if (!out) return FKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  fkv_status s = check_config(cfg);
+  if (s != FKV_OK) return s;
+  fkv_ctx* c = new (std::nothrow) fkv_ctx();
+  if (!c) return FKV_ERR_INVALID_ARG;
+  c->cfg = *cfg;
+  c->n = cfg->num_layers / 2;
+  c->group = cfg->num_q_heads / cfg->num_kv_heads;
+  c->scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0f / std::sqrt((float)cfg->head_dim);
+  c->k.assign(cfg->num_layers + 1, nullptr);
+  c->v.assign(cfg->num_layers + 1, nullptr);
+  for (auto& w : c->w) w.assign(cfg->num_layers + 1, nullptr);
+  c->status = nullptr;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
+      cudaMalloc(&c->status, sizeof(int)) != cudaSuccess ||
+      cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    if (c->status) cudaFree(c->status);
+    delete c;
+    return FKV_ERR_CUDA;
+  }
+  *out = c;
+  return FKV_OK;
+}
+
+void fkv_destroy(fkv_ctx* c) {
+  if (!c) return;
+  if (c->status) cudaFree(c->status);
+  delete c;
+}
+
+fkv_status fkv_bind_layer_cache(fkv_ctx* c, int layer, void* k, void* v) {
+  if (!c || layer < 1 || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
+  if (layer > c->n && !c->cfg.store_upper) return FKV_ERR_UNSUPPORTED;
+  if (!k || !v || !aligned16(k) || !aligned16(v)) return FKV_ERR_INVALID_ARG;
+  c->k[layer] = k;
+  c->v[layer] = v;
+  return FKV_OK;
+}
+
+fkv_status fkv_set_fusion_weights(fkv_ctx* c, int layer, const float* a_first,
+                                  const float* a_second, const float* b_first,
+                                  const float* b_second) {
+  if (!c || layer <= c->n || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
+  const float* ws[4] = {a_first, a_second, b_first, b_second};
+  for (int i = 0; i < 4; ++i)
+    if (!ws[i] || !aligned16(ws[i])) return FKV_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i) c->w[i][layer] = ws[i];
+  return FKV_OK;
+}
+
+fkv_status fkv_append_kv(fkv_ctx* c, int layer, const void* k_new, const void* v_new,
+                         const int32_t* pos, int T, void* stream) {
+  if (!c || layer < 1 || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
+  if (layer > c->n && !c->cfg.store_upper) return FKV_ERR_UNSUPPORTED;
+  if (T < 0 || T > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
+  if (!c->k[layer] || !c->v[layer]) return FKV_ERR_INVALID_ARG;
+  if (T == 0) return FKV_OK;
+  if (!k_new || !v_new || !pos || !aligned16(k_new) || !aligned16(v_new) ||
+      (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return FKV_ERR_INVALID_ARG;
+  fkv::AppendArgs a{};
+  a.k_cache = c->k[layer];
+  a.v_cache = c->v[layer];
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.pos = pos;
+  a.status = c->status;
+  a.batch = c->cfg.batch;
+  a.kv_heads = c->cfg.num_kv_heads;
+  a.max_seq = c->cfg.max_seq;
+  a.head_dim = c->cfg.head_dim;
+  a.T = T;
+  a.elem_bytes = elem_bytes(c->cfg);
+  return fkv::append_launch(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FKV_OK
+                                                                                 : FKV_ERR_CUDA;
+}
+
+size_t fkv_decode_workspace_bytes(const fkv_ctx* c) {
+  if (!c) return 0;
+  size_t best = 0;
+  for (int nsrc = 1; nsrc <= 2; ++nsrc) {
+    fkv::DecodeArgs d = decode_args(c);
+    d.nsrc = nsrc;
+    fkv::DecodePlan p{};
+    if (fkv::decode_plan(d, c->num_sms, &p) == cudaSuccess && p.workspace_bytes > best)
+      best = p.workspace_bytes;
+  }
+  return best;
+}
+
+fkv_status fkv_decode_attn(fkv_ctx* c, const void* q, int layer, int mode,
+                           const int32_t* seq_lens, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!c) return FKV_ERR_INVALID_ARG;
+  fkv::DecodeArgs d = decode_args(c);
+  fkv_status s = resolve_sources(c, layer, mode, d.k, d.v, d.a, d.b, &d.nsrc);
+  if (s != FKV_OK) return s;
+  if (!q || !out || !seq_lens || !aligned16(q) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return FKV_ERR_INVALID_ARG;
+  fkv::DecodePlan plan{};
+  if (fkv::decode_plan(d, c->num_sms, &plan) != cudaSuccess) return FKV_ERR_UNSUPPORTED;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < plan.workspace_bytes)
+    return FKV_ERR_WORKSPACE;
+  d.q = q;
+  d.out = out;
+  d.seq_lens = seq_lens;
+  d.workspace = static_cast<float*>(workspace);
+  return fkv::decode_launch(d, plan, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FKV_OK
+             : FKV_ERR_CUDA;
+}
+
+fkv_status fkv_prefill_attn(fkv_ctx* c, const void* q, int layer, int mode, int S, void* out,
+                            void* stream) {
+  if (!c) return FKV_ERR_INVALID_ARG;
+  fkv::PrefillArgs p{};
+  fkv_status s = resolve_sources(c, layer, mode, p.k, p.v, p.a, p.b, &p.nsrc);
+  if (s != FKV_OK) return s;
+  if (c->cfg.dtype != FKV_BF16) return FKV_ERR_UNSUPPORTED;
+  if (S < 1 || S > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return FKV_ERR_INVALID_ARG;
+  p.q = q;
+  p.out = out;
+  p.status = c->status;
+  p.batch = c->cfg.batch;
+  p.kv_heads = c->cfg.num_kv_heads;
+  p.group = c->group;
+  p.max_seq = c->cfg.max_seq;
+  p.head_dim = c->cfg.head_dim;
+  p.S = S;
+  p.softmax_scale = c->scale;
+  const cudaError_t e = fkv::prefill_launch(p, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return FKV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
+}
+
+fkv_status fkv_get_device_status(fkv_ctx* c, void* stream) {
+  if (!c) return FKV_ERR_INVALID_ARG;
+  int h = 0;
+  if (cudaMemcpyAsync(&h, c->status, sizeof(int), cudaMemcpyDeviceToHost,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FKV_ERR_CUDA;
+  }
+  if (h == 0) return FKV_OK;
+  if (cudaMemsetAsync(c->status, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FKV_ERR_CUDA;
+  return (h & fkv::kDevTimeoutBit) ? FKV_ERR_TIMEOUT : FKV_ERR_DEVICE_ARG;
+}
+
+const char* fkv_status_string(fkv_status s) {
+  switch (s) {
+    case FKV_OK: return "ok";
+    case FKV_ERR_INVALID_ARG: return "invalid argument";
+    case FKV_ERR_UNSUPPORTED: return "unsupported";
+    case FKV_ERR_CUDA: return "CUDA error";
+    case FKV_ERR_TIMEOUT: return "device wait timed out";
+    case FKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case FKV_ERR_DEVICE_ARG: return "device saw an out-of-range length or position";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

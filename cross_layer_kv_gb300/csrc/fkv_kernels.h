@@ -1,0 +1,79 @@
+// Host-visible launch interfaces of the FusedKV kernels (internal to the
+// library; the public ABI is include/fusedkv.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fkv {
+
+// One decode attention call, after host validation.  Pointers are device
+// pointers.  nsrc = 1: K from k[0], V from v[0] (vanilla or lite);
+// nsrc = 2: fused, K = a0 (.) k[0] + a1 (.) k[1], V = b0 (.) v[0] + b1 (.) v[1].
+struct DecodeArgs {
+  const void* k[2];
+  const void* v[2];
+  const float* a[2];
+  const float* b[2];
+  const void* q;             // [B, H_q, D]
+  void* out;                 // [B, H_q, D]
+  const int32_t* seq_lens;   // [B]
+  float* workspace;          // split partials
+  int* status;               // device status word
+  int batch, kv_heads, group, max_seq, head_dim;
+  int nsrc;
+  int is_f32;
+  float softmax_scale;
+  int num_ctas;              // split grid (0 = library default)
+};
+
+// Launch configuration the library picks for a decode call shape.
+struct DecodePlan {
+  int ctas;          // CTAs of the split kernel
+  int warps_per_cta;
+  size_t smem_bytes;
+  size_t workspace_bytes;
+};
+
+// Plan (grid and workspace) for a shape; num_sms from the device.
+cudaError_t decode_plan(const DecodeArgs& a, int num_sms, DecodePlan* plan);
+
+// Launch split kernel + merge kernel on `stream`.
+cudaError_t decode_launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+
+// Number of kernel launches one decode call makes (for launch accounting).
+constexpr int kDecodeLaunchesPerCall = 2;
+
+struct AppendArgs {
+  void* k_cache;
+  void* v_cache;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* pos;
+  int* status;
+  int batch, kv_heads, max_seq, head_dim, T, elem_bytes;
+};
+
+cudaError_t append_launch(const AppendArgs& a, cudaStream_t stream);
+
+constexpr int kDevTimeoutBit = 2;  // must match kDevTimeout
+
+struct PrefillArgs {
+  const void* k[2];
+  const void* v[2];
+  const float* a[2];
+  const float* b[2];
+  const void* q;   // [B, H_q, S, D] bf16
+  void* out;       // [B, H_q, S, D] bf16
+  int* status;
+  int batch, kv_heads, group, max_seq, head_dim, S;
+  int nsrc;
+  float softmax_scale;
+};
+
+// Returns cudaErrorNotSupported for shapes the tensor-core kernel does not
+// cover.
+cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace fkv

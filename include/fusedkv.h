@@ -1,0 +1,159 @@
+/*
+ * fusedkv.h -- C ABI of the FusedKV attention library for GB300 (sm_103a).
+ *
+ * FusedKV ("Reconstructing KV Caches with Cross-Layer Fusion for Enhanced
+ * Transformers", Lin et al., arXiv:2512.03870) keeps post-RoPE K/V caches only
+ * for the lower half of the layers.  With L = 2n layers (1-based):
+ *
+ *   storage layers        1..n    attend over their own stored K/V;
+ *   reconstruction layers n+1..L  rebuild K/V on demand from layers 1 and n:
+ *     fused (FusedKV slides, Eqs.(4)-(5)):
+ *        K^i = a_{i,1} (.) K^1 + a_{i,n} (.) K^n
+ *        V^i = b_{i,1} (.) V^1 + b_{i,n} (.) V^n
+ *     lite  (FusedKV slides, Eq.(6)):  K^i = K^n,  V^i = V^1
+ *     vanilla (Table 1, the full-cache baseline): every layer stores its own.
+ *
+ * The reconstruction happens inside the attention kernels; reconstructed upper
+ * layer K/V is never written to memory (FusedKV slides, Table 1 slide: "fuse on
+ * demand"; reading notes §2.3).
+ *
+ * Conventions used by every call:
+ *   - Layers are 1-based, L even, n = L / 2 (reading notes §2.1, Eq.(1)).
+ *   - Caches are caller-owned device buffers, contiguous [B, H_kv, S_max, D],
+ *     holding post-RoPE keys and values; element type = the context dtype.
+ *   - Fusion weights are caller-owned device fp32 buffers [H_kv, D] per
+ *     target layer (one weight per KV head and channel, broadcast over batch
+ *     and tokens).  The key weights should be tied across each RoPE rotation
+ *     pair (channel j with j + D/2 in rotate-half storage; FusedKV slides,
+ *     Eqs.(7)-(8)); the library does not enforce it.
+ *   - GQA: query head h reads KV head h / (H_q / H_kv).
+ *   - Softmax scale: config.softmax_scale, or 1/sqrt(D) when it is 0.
+ *   - Device pointers must be 16-byte aligned.
+ *   - Every call is asynchronous and ordered on the given stream (a
+ *     cudaStream_t passed as void*; NULL = the legacy default stream).
+ *   - Host-side validation happens before any launch; a failing call
+ *     launches nothing.  Conditions only the device can see (a sequence
+ *     length out of range, a bounded wait that ran out) are recorded in a
+ *     device status word read by fkv_get_device_status().
+ *   - Nothing aborts, throws or allocates on the hot path; the library owns
+ *     only its context (and, after fkv_create, one 4-byte device status word).
+ */
+#ifndef FUSEDKV_H_
+#define FUSEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FKV_OK = 0,
+  FKV_ERR_INVALID_ARG = 1,  /* bad pointer, size, layer, alignment or config */
+  FKV_ERR_UNSUPPORTED = 2,  /* valid request this build or config cannot serve */
+  FKV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  FKV_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out */
+  FKV_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
+  FKV_ERR_DEVICE_ARG = 6    /* device saw a sequence length / position out of range */
+} fkv_status;
+
+typedef enum { FKV_VANILLA = 0, FKV_LITE = 1, FKV_FUSED = 2 } fkv_mode;
+
+typedef enum { FKV_BF16 = 0, FKV_F32 = 1 } fkv_dtype;
+
+typedef struct {
+  int num_layers;     /* L, even, >= 2 */
+  int batch;          /* B, 1..1024 */
+  int max_seq;        /* S_max: cache rows per (batch, KV head) */
+  int num_q_heads;    /* H_q, a multiple of H_kv, H_q / H_kv in {1, 2, 4} */
+  int num_kv_heads;   /* H_kv */
+  int head_dim;       /* D in {64, 80, 96, 128} */
+  int dtype;          /* fkv_dtype of caches, queries and outputs */
+  int store_upper;    /* 1: upper layers also keep their own caches, so that
+                         vanilla attention can run on them (comparison path) */
+  float softmax_scale;/* 0 => 1/sqrt(D) */
+  int decode_ctas;    /* 0: the library picks the decode split grid (one CTA
+                         per SM, fewer for short caches); > 0 forces that
+                         many CTAs (results agree up to fp32 rounding) */
+} fkv_config;
+
+typedef struct fkv_ctx fkv_ctx;
+
+/* Create a context for the current CUDA device.  Validates the config
+ * (FKV_ERR_INVALID_ARG / FKV_ERR_UNSUPPORTED before touching CUDA), then
+ * queries the device and allocates the 4-byte status word (FKV_ERR_CUDA on
+ * failure, e.g. no GPU).  *out is set to NULL on any error. */
+fkv_status fkv_create(const fkv_config* cfg, fkv_ctx** out);
+
+/* Free the context and its status word.  NULL is ignored.  Does not touch
+ * caller buffers. */
+void fkv_destroy(fkv_ctx* ctx);
+
+/* Register the K and V cache buffers of a layer (device, [B,H_kv,S_max,D],
+ * 16-byte aligned).  Storage layers 1..n always have caches; upper layers only
+ * when config.store_upper is set (else FKV_ERR_UNSUPPORTED: upper layers store
+ * nothing, reading notes §2.1).  The buffers stay owned by the caller and must
+ * outlive their use. */
+fkv_status fkv_bind_layer_cache(fkv_ctx* ctx, int layer, void* k, void* v);
+
+/* Register the fusion weights of reconstruction layer n < layer <= L
+ * (FusedKV slides, Eqs.(4)-(5)): a_first/a_second scale K^1/K^n, b_first/
+ * b_second scale V^1/V^n.  Each is a device fp32 [H_kv, D] buffer owned by the
+ * caller.  Any sign and any sum are allowed. */
+fkv_status fkv_set_fusion_weights(fkv_ctx* ctx, int layer, const float* a_first,
+                                  const float* a_second, const float* b_first,
+                                  const float* b_second);
+
+/* Write the post-RoPE K/V of T new tokens into a layer's cache (the storage
+ * caches take the new token before the upper layers attend; reading notes
+ * §2.3).  k_new, v_new: device [B, H_kv, T, D] in the context dtype.
+ * pos: device int32 [B], first cache row to write for each sequence.
+ * Rows pos[b]..pos[b]+T-1 of every KV head are written; a sequence whose rows
+ * fall outside [0, S_max) is skipped and flagged as FKV_ERR_DEVICE_ARG in the
+ * device status.  The layer must have a bound cache. */
+fkv_status fkv_append_kv(fkv_ctx* ctx, int layer, const void* k_new, const void* v_new,
+                         const int32_t* pos, int T, void* stream);
+
+/* Bytes of device workspace fkv_decode_attn needs for this context (split-K
+ * partial results).  The caller allocates it; its contents need no
+ * initialisation and may be reused by every decode call on the same stream. */
+size_t fkv_decode_workspace_bytes(const fkv_ctx* ctx);
+
+/* One decode attention call of a layer (a single query position per sequence).
+ * q: device [B, H_q, D]; out: device [B, H_q, D]; both in the context dtype.
+ * seq_lens: device int32 [B]; sequence b attends over cache rows
+ * [0, seq_lens[b]) (the new token already appended).  A length outside
+ * [1, S_max] is clamped (0 yields a zero output) and flagged as
+ * FKV_ERR_DEVICE_ARG in the device status.
+ * mode: for storage layers every mode is plain attention over the layer's own
+ * cache; for upper layers FKV_VANILLA reads the layer's own cache (needs
+ * store_upper), FKV_LITE reads K^n and V^1, FKV_FUSED reads K^1, K^n, V^1, V^n
+ * with the layer's weights and fuses them in registers.
+ * workspace: device, at least fkv_decode_workspace_bytes(ctx) bytes. */
+fkv_status fkv_decode_attn(fkv_ctx* ctx, const void* q, int layer, int mode,
+                           const int32_t* seq_lens, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Causal prefill attention of a layer over a prompt occupying cache rows
+ * [0, S) of every sequence (the storage caches already hold those rows).
+ * q: device [B, H_q, S, D]; out: device [B, H_q, S, D]; context dtype.
+ * Query row m sees key rows t <= m.  Modes and sources as for decode; fused
+ * K/V tiles are built while staging them for the tensor cores.
+ * Requires dtype FKV_BF16 (FKV_ERR_UNSUPPORTED otherwise); 1 <= S <= S_max. */
+fkv_status fkv_prefill_attn(fkv_ctx* ctx, const void* q, int layer, int mode, int S,
+                            void* out, void* stream);
+
+/* Synchronise the stream, then report and clear the device status word:
+ * FKV_OK, FKV_ERR_DEVICE_ARG or FKV_ERR_TIMEOUT (FKV_ERR_CUDA if the sync
+ * itself fails). */
+fkv_status fkv_get_device_status(fkv_ctx* ctx, void* stream);
+
+/* A static, human-readable name of a status code. */
+const char* fkv_status_string(fkv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSEDKV_H_ */

@@ -1,0 +1,176 @@
+"""GPU parity of fkv_decode_attn against the float64 oracle, through the C ABI.
+
+Small cases compare every output element; the full-size workloads (the
+launch configuration the benchmark times) compare sampled (batch, head) rows
+that the oracle computes one at a time."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from cross_layer_kv_gb300 import synth
+from cross_layer_kv_gb300 import fusedkv as B
+from parity import DecodeSetup, assert_close, f64
+
+pytestmark = pytest.mark.gpu
+
+MODES = ("vanilla", "lite", "fused")
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    yield
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("layer", [1, 2, 3, 4])
+def test_tiny_fp32_all_layers(mode, layer):
+    """L=4, B=1, S=256, 4 Q / 2 KV heads, D=64, fp32, seed 0: max-abs 1e-5."""
+    s = DecodeSetup(synth.TINY, layer, [mode])
+    got = f64(s.run(mode))
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    assert_close(got, s.oracle(mode), "f32", "tiny %s layer %d" % (mode, layer))
+    s.close()
+
+
+def _small(D, G, dtype="bf16", S=700, Bt=3, L=6):
+    return synth.Workload("small", L, Bt, S, 2 * G, 2, D, dtype)
+
+
+@pytest.mark.parametrize("D", [64, 80, 96, 128])
+@pytest.mark.parametrize("G", [1, 2, 4])
+@pytest.mark.parametrize("mode", MODES)
+def test_small_bf16_ragged(D, G, mode):
+    w = _small(D, G)
+    lens = [700, 1, 333]
+    s = DecodeSetup(w, 5, [mode], seed=3, lens=lens)
+    got = f64(s.run(mode))
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    assert_close(got, s.oracle(mode), "bf16", "D=%d G=%d %s" % (D, G, mode))
+    s.close()
+
+
+@pytest.mark.parametrize("D", [80, 128])
+@pytest.mark.parametrize("mode", ["lite", "fused"])
+def test_small_fp32(D, mode):
+    w = _small(D, 2, dtype="f32", S=513, Bt=2)
+    s = DecodeSetup(w, 6, [mode], seed=4, lens=[513, 77])
+    assert_close(f64(s.run(mode)), s.oracle(mode), "f32", "fp32 D=%d %s" % (D, mode))
+    s.close()
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 5, 37])
+def test_split_count_invariance(ctas):
+    """Any split grid gives the oracle's answer (fused, ragged)."""
+    w = _small(64, 2, S=2048, Bt=5)
+    lens = [2048, 1500, 9, 1024, 1]
+    s = DecodeSetup(w, 4, ["fused"], seed=5, lens=lens, decode_ctas=ctas)
+    assert_close(f64(s.run("fused")), s.oracle("fused"), "bf16", "ctas=%d" % ctas)
+    s.close()
+
+
+def test_more_warps_than_rows():
+    """A grid with more warps than cache rows (empty warp ranges)."""
+    w = _small(64, 2, S=16, Bt=2)
+    s = DecodeSetup(w, 4, ["fused", "lite"], seed=6, lens=[3, 5], decode_ctas=64)
+    for m in ("fused", "lite"):
+        assert_close(f64(s.run(m)), s.oracle(m), "bf16", m)
+    s.close()
+
+
+def test_lite_equals_fused_with_zero_one_weights():
+    """Lite (K^n, V^1) and fused with (a1, an, b1, bn) = (0, 1, 1, 0) agree."""
+    w = _small(96, 2, S=1000, Bt=2)
+    s = DecodeSetup(w, 4, ["lite", "fused"], seed=7, lens=[1000, 640])
+    z = torch.zeros_like(s.weights[0])
+    o = torch.ones_like(s.weights[0])
+    s.ctx.fkv_set_fusion_weights(4, z, o, o, z)
+    lite = f64(s.run("lite")).copy()
+    fused = f64(s.run("fused"))
+    assert np.max(np.abs(lite - fused)) <= 1e-2
+    assert_close(fused, s.oracle("lite"), "bf16", "fused(0,1,1,0) vs lite oracle")
+    s.close()
+
+
+def test_untied_and_negative_weights():
+    """Weights of any sign, untied across RoPE pairs, are used as given."""
+    w = _small(64, 2, S=300, Bt=2)
+    s = DecodeSetup(w, 6, ["fused"], seed=8, lens=[300, 299], tie_keys=False, weight_std=1.5)
+    s.weights[2].neg_()
+    assert_close(f64(s.run("fused")), s.oracle("fused"), "bf16", "untied")
+    s.close()
+
+
+def test_out_of_range_lengths_flagged():
+    """Length 0 gives a zero row, a length above S_max is clamped; both set
+    FKV_ERR_DEVICE_ARG in the device status, the other rows stay correct."""
+    w = _small(64, 2, S=256, Bt=3)
+    s = DecodeSetup(w, 5, ["fused"], seed=9, lens=[0, 9999, 100])
+    got = f64(s.run("fused"))
+    assert s.ctx.fkv_get_device_status() == B.FKV_ERR_DEVICE_ARG
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK  # cleared
+    assert np.all(got[0] == 0)
+    s.lens = torch.tensor([1, 256, 100], dtype=torch.int32, device="cuda")
+    ref = s.oracle("fused")
+    assert_close(got[1:], ref[1:], "bf16", "clamped")
+    s.close()
+
+
+def test_host_validation_launches_nothing():
+    w = _small(64, 2, S=64, Bt=1)
+    s = DecodeSetup(w, 4, ["fused"], seed=10, lens=[64])
+    with pytest.raises(B.FkvError) as e:
+        s.ctx.fkv_decode_attn(s.q, 4, "fused", s.lens, s.out, s.ws[:16])
+    assert e.value.status == B.FKV_ERR_WORKSPACE
+    with pytest.raises(B.FkvError) as e:
+        s.ctx.fkv_decode_attn(s.q, 4, "vanilla", s.lens, s.out, s.ws)   # no own cache
+    assert e.value.status == B.FKV_ERR_UNSUPPORTED
+    with pytest.raises(B.FkvError) as e:
+        s.ctx.fkv_decode_attn(s.q, 7, "fused", s.lens, s.out, s.ws)
+    assert e.value.status == B.FKV_ERR_INVALID_ARG
+    with pytest.raises(B.FkvError) as e:
+        s.ctx.fkv_decode_attn(s.q.data_ptr() + 2, 4, "fused", s.lens, s.out, s.ws)
+    assert e.value.status == B.FKV_ERR_INVALID_ARG
+    s.close()
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled rows
+# ---------------------------------------------------------------------------
+
+def _pairs(w, k, seed):
+    rng = np.random.default_rng(seed)
+    bs = rng.integers(0, w.batch, k)
+    hs = rng.integers(0, w.q_heads, k)
+    pairs = sorted(set(zip(bs.tolist(), hs.tolist())))
+    return pairs + [(0, 0), (w.batch - 1, w.q_heads - 1)]
+
+
+@pytest.mark.parametrize("w", [synth.M332, synth.B1_5, synth.B4], ids=lambda w: w.name)
+@pytest.mark.parametrize("mode", MODES)
+def test_full_size_sampled(w, mode):
+    layer = w.num_layers  # the top reconstruction layer
+    s = DecodeSetup(w, layer, [mode], seed=0)
+    got = f64(s.run(mode))
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    pairs = _pairs(w, 6, 11)
+    ref = s.oracle(mode, pairs)
+    sel = np.stack([got[b, h] for b, h in pairs])
+    assert_close(sel, ref, "bf16", "%s %s" % (w.name, mode))
+    s.close()
+    torch.cuda.empty_cache()
+
+
+def test_full_size_storage_layer():
+    w = synth.M332
+    s = DecodeSetup(w, 1, ["fused"], seed=0)
+    got = f64(s.run("fused"))
+    pairs = _pairs(w, 4, 12)
+    assert_close(np.stack([got[b, h] for b, h in pairs]), s.oracle("fused", pairs), "bf16",
+                 "storage layer 1")
+    s.close()
