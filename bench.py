@@ -341,6 +341,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=4.0)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    help="run one call type only, e.g. decode:fused:332M-decode or "
+                         "prefill:fused:650M-prefill (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -361,6 +364,9 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    if args.profile:
+        run_profile_case(args, device)
+        return
     if dist_on:
         torch.distributed.init_process_group("nccl", device_id=device)
 
@@ -380,15 +386,20 @@ def main():
     for mode in ("vanilla", "lite", "fused"):
         if mode == "fused":
             with ClockSampler(local) as cs:
-                ms, upper_ms = time_steps(model, mode, K, W, stream, dist_on, device,
-                                          collect_upper=True)
+                ms, up = time_steps(model, mode, K, W, stream, dist_on, device,
+                                    collect_upper=True)
             clocks = cs.summary()
             launches = K * model.launches_per_step(mode)
+            upper_ms = up
         else:
-            ms, _ = time_steps(model, mode, K, W, stream, dist_on, device)
+            ms, up = time_steps(model, mode, K, W, stream, dist_on, device, collect_upper=True)
         step_ms = ms / K
         gb = model.step_bytes(mode) / 1e9
+        ub = model.call_bytes(w.num_layers, mode) / 1e9
         modes[mode] = {
+            "upper_call_us": up * 1e3,
+            "upper_call_GBps": ub / (up / 1e3),
+            "upper_call_pct_of_8TBps": 100.0 * ub / (up / 1e3) / HBM_REF_GBS,
             "tokens_per_s": w.batch * world / (step_ms / 1e3),
             "step_ms": step_ms,
             "step_bytes_GB": gb,
@@ -460,6 +471,60 @@ def main():
         print(json.dumps(line), flush=True)
     if dist_on:
         torch.distributed.destroy_process_group()
+
+
+def run_profile_case(args, device):
+    """One call type on its own, W warm-up calls then K timed calls; prints
+    the mean call time.  Used for ncu captures of a single kernel."""
+    import cross_layer_kv_gb300 as fkv
+    from cross_layer_kv_gb300 import synth
+    kind, mode, wname = args.profile.split(":")
+    w = synth.WORKLOADS[wname]
+    layer = w.num_layers
+    n = w.n
+    need = [layer] if mode == "vanilla" else sorted({1, n})
+    ctx = fkv.Context(w.num_layers, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim, w.dtype,
+                      store_upper=(mode == "vanilla"))
+    keep = []
+    for l in need:
+        k, v = synth.make_cache(w, l, 0, device)
+        keep.append((k, v))
+        ctx.fkv_bind_layer_cache(l, k, v)
+    wts = synth.make_weights(w, layer, 0, device)
+    ctx.fkv_set_fusion_weights(layer, *wts)
+    stream = torch.cuda.Stream(device)
+    if kind == "decode":
+        q = synth.make_query(w, layer, 0, device)
+        out = torch.empty_like(q)
+        lens = synth.make_seq_lens(w, 0, device)
+        ws = ctx.workspace(device)
+        call = lambda: ctx.fkv_decode_attn(q, layer, mode, lens, out, ws, stream)
+        nbytes = (4 if mode == "fused" else 2) * w.kv_heads * int(lens.sum()) * w.head_dim * w.elem_bytes
+    else:
+        q = synth.make_query(w, layer, 0, device, positions=w.seq)
+        out = torch.empty_like(q)
+        call = lambda: ctx.fkv_prefill_attn(q, layer, mode, w.seq, out, stream)
+        nbytes = 0
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    res = {"profile": args.profile, "call_us": us}
+    if nbytes:
+        res["GBps"] = nbytes / (us * 1e-6) / 1e9
+        res["bytes"] = nbytes
+    else:
+        flops = 4.0 * w.batch * w.q_heads * w.head_dim * w.seq * (w.seq + 1) / 2
+        res["TFLOPs"] = flops / (us * 1e-6) / 1e12
+    print(json.dumps(res), flush=True)
+    ctx.close()
 
 
 def bench_prefill(device, stream, peaks, W):

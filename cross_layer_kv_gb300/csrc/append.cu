@@ -10,6 +10,8 @@
 namespace fkv {
 
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  grid_dep_trigger();
+  grid_dep_wait();
   const int chunks = a.head_dim * a.elem_bytes / 16;   // 16-byte chunks per row
   const long long per_seq = (long long)a.kv_heads * a.T * chunks;
   const long long total = (long long)a.batch * per_seq;
@@ -38,8 +40,7 @@ cudaError_t append_launch(const AppendArgs& a, cudaStream_t stream) {
   if (total == 0) return cudaSuccess;
   long long blocks = (total + 255) / 256;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, a);
 }
 
 }  // namespace fkv

@@ -119,31 +119,6 @@ struct RowWalker {
   }
 };
 
-template <typename T>
-__device__ __forceinline__ void unpack16(const uint4& w, float* f);
-
-template <>
-__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4& w, float* f) {
-  f[0] = bf16lo(w.x); f[1] = bf16hi(w.x);
-  f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
-  f[4] = bf16lo(w.z); f[5] = bf16hi(w.z);
-  f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
-}
-
-template <>
-__device__ __forceinline__ void unpack16<float>(const uint4& w, float* f) {
-  f[0] = __uint_as_float(w.x);
-  f[1] = __uint_as_float(w.y);
-  f[2] = __uint_as_float(w.z);
-  f[3] = __uint_as_float(w.w);
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Sum over the C lanes of each row group; every lane of the group gets it.
 template <int C>
 __device__ __forceinline__ float group_sum(float v, int lane) {
@@ -190,6 +165,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
 
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) mbar_init(&bars[warp * NS + s], 1);
+    fence_mbar_init();
+  }
+  grid_dep_trigger();
+  grid_dep_wait();
+
   // Sequence lengths, clamped to [0, S_max]; one CTA reports bad ones.
   for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
     int L = p.seq_lens[i];
@@ -198,11 +181,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       L = L < 0 ? 0 : (L > p.S_max ? p.S_max : L);
     }
     lens[i] = L;
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < NS; ++s) mbar_init(&bars[warp * NS + s], 1);
-    fence_mbar_init();
   }
   __syncthreads();
   if (warp == 0) {
@@ -478,6 +456,8 @@ template <typename T>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  grid_dep_trigger();
+  grid_dep_wait();
   const int Hq = p.H_kv * p.G;
   if (row >= (long long)p.B * Hq) return;
   const int b = (int)(row / Hq), hq = (int)(row % Hq);
@@ -574,8 +554,7 @@ cudaError_t decode_launch_t(const DecodeArgs& a, const DecodePlan& plan, cudaStr
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem_bytes);
   if (e != cudaSuccess) return e;
-  kern<<<plan.ctas, kDecodeWarps * 32, plan.smem_bytes, stream>>>(sp);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3(plan.ctas), dim3(kDecodeWarps * 32), plan.smem_bytes, stream, sp);
   if (e != cudaSuccess) return e;
 
   MergeParams mp;
@@ -590,8 +569,8 @@ cudaError_t decode_launch_t(const DecodeArgs& a, const DecodePlan& plan, cudaStr
   mp.total_warps = plan.ctas * kDecodeWarps;
   mp.is_f32 = sizeof(T) == 4;
   const long long rows = (long long)a.batch * a.kv_heads * G;
-  decode_merge_kernel<T><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(mp);
-  return cudaGetLastError();
+  return launch_pdl(decode_merge_kernel<T>, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, stream,
+                    mp);
 }
 
 }  // namespace fkv

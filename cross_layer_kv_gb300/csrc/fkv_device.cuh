@@ -20,6 +20,18 @@ enum : int {
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr unsigned long long kDrainLimitNs = 50000000ull;   // 50 ms
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor in the stream is still
+// running.  grid_dep_wait() blocks until the predecessor grid has completed and
+// its memory is visible, so every kernel calls it before its first global
+// memory access; grid_dep_trigger() lets the successor be scheduled early.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -115,5 +127,30 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // bf16 pair in a 32-bit word -> two fp32 (exact: bf16 is the top half of fp32).
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& w, float* f);
+
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4& w, float* f) {
+  f[0] = bf16lo(w.x); f[1] = bf16hi(w.x);
+  f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+  f[4] = bf16lo(w.z); f[5] = bf16hi(w.z);
+  f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+}
+
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4& w, float* f) {
+  f[0] = __uint_as_float(w.x);
+  f[1] = __uint_as_float(w.y);
+  f[2] = __uint_as_float(w.z);
+  f[3] = __uint_as_float(w.w);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 }  // namespace fkv

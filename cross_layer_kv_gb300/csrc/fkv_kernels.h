@@ -45,6 +45,23 @@ cudaError_t decode_launch(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
 // Number of kernel launches one decode call makes (for launch accounting).
 constexpr int kDecodeLaunchesPerCall = 2;
 
+// Launch `kern` with programmatic stream serialization (see grid_dep_wait).
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 struct AppendArgs {
   void* k_cache;
   void* v_cache;

@@ -1,4 +1,560 @@
+// Causal prefill attention for FusedKV upper layers (and the vanilla / Lite
+// paths) on the 5th-generation tensor cores of sm_103a.
+//
+// What one call computes: for every sequence b, query head h (KV head
+// kh = h / G) and query position m < S
+//     o_{h,m} = sum_{t <= m} softmax_t(scale * q_{h,m} . K_t) V_t
+// with K/V the layer's own cache (vanilla), K^n / V^1 (lite, FusedKV slides
+// Eq.(6)) or a_1 (.) K^1 + a_n (.) K^n and b_1 (.) V^1 + b_n (.) V^n (fused,
+// Eqs.(4)-(5)), built tile by tile in shared memory and never written to
+// global memory (Table 1 slide: fuse on demand; reading notes §2.3).
+//
+// Structure of one CTA: one 128-row query tile of one (b, kh) unit and all G
+// query heads of that KV head (one warpgroup per head).
+//  * TMA (cp.async.bulk.tensor, 64-byte swizzle) loads the Q tiles once and the
+//    K/V source tiles of 64 keys into a 2-stage ring; the loads of tile j+2
+//    overlap the work on tile j.
+//  * Fused mode: the warps combine the two sources of each K and V tile in
+//    fp32 and write the bf16 result in place, in the same swizzled layout the
+//    tensor cores read (the fused tile is shared by all G heads).
+//  * One thread issues tcgen05.mma: S_h = Q_h K^T into tensor memory, then,
+//    after the softmax warps have written P_h (bf16) to shared memory,
+//    O_h += P_h V, also accumulated in tensor memory.
+//  * Softmax: each thread owns one query row (one TMEM lane), reads its S row
+//    with tcgen05.ld, applies the causal mask and the online (base-2) softmax,
+//    rescales its O row in tensor memory when the running max grows.
+//  * Every wait is bounded; a wait that runs out flags the device status,
+//    releases the tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cfloat>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fkv_device.cuh"
 #include "fkv_kernels.h"
+
 namespace fkv {
-cudaError_t prefill_launch(const PrefillArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int BM = 128;       // query rows per CTA
+constexpr int BN = 64;        // keys per tile
+constexpr int SW = 64;        // swizzle span in bytes (32 bf16)
+constexpr int SWE = SW / 2;   // elements per swizzle row
+constexpr int TMEM_COLS = 512;
+constexpr int HEAD_COLS = 256;  // TMEM columns per head: S (BN) then O (D)
+
+// --- tcgen05 / TMA wrappers --------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of tcgen05 (start, leading and stride byte
+// offsets, descriptor version 1, swizzle mode 4 = 64-byte swizzle).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B,
+// A K-major, B K-major or MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Byte offset of the 16-byte chunk `lc` of row `r` inside one 64-byte-swizzled
+// block whose rows are 64 bytes (the pattern TMA writes and the MMA reads).
+__device__ __forceinline__ uint32_t swz64(int r, int lc) {
+  return (uint32_t)(r * SW + ((lc ^ ((r >> 1) & 3)) << 4));
+}
+
+template <int D>
+struct PrefillCfg {
+  static constexpr int CB = (D + SWE - 1) / SWE;    // 32-element column blocks
+  static constexpr int Q_BYTES = CB * BM * SW;      // one head's Q tile
+  static constexpr int KV_BYTES = CB * BN * SW;     // one K or V source tile
+  static constexpr int P_BYTES = (BN / SWE) * BM * SW;
+};
+
+struct PrefillParams {
+  const float* a0;
+  const float* a1;
+  const float* b0;
+  const float* b1;
+  void* out;
+  int* status;
+  int B, H_kv, S;
+  float scale_log2;
+};
+
+struct PrefillMaps {
+  CUtensorMap q;
+  CUtensorMap k0, k1, v0, v1;
+};
+
+template <int D, int NSRC, int G>
+size_t prefill_smem_bytes() {
+  using Cfg = PrefillCfg<D>;
+  size_t s = (size_t)G * Cfg::Q_BYTES + 2ull * 2 * NSRC * Cfg::KV_BYTES + (size_t)G * Cfg::P_BYTES;
+  s += 4 * D * sizeof(float);  // fusion weights
+  s += 64;                     // barriers + TMEM slot
+  s += 512;                    // alignment slack
+  // at least 116 KB so that one CTA holds an SM (it takes all 512 TMEM columns)
+  return s < 118784 ? 118784 : s;
+}
+
+template <int D, int NSRC, int G>
+__global__ void __launch_bounds__(128 * G, 1)
+    prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillParams p) {
+  using Cfg = PrefillCfg<D>;
+  constexpr int CB = Cfg::CB;
+  constexpr int NT = 128 * G;
+  extern __shared__ uint8_t smem_raw[];
+  // 512-byte alignment: the period of the 64-byte swizzle pattern
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 511) &
+                                             ~uintptr_t(511));
+  uint8_t* sQ = smem;                                     // G x Q tile
+  uint8_t* sKV = sQ + G * Cfg::Q_BYTES;                   // 2 stages x (K srcs, V srcs)
+  uint8_t* sP = sKV + 2 * 2 * NSRC * Cfg::KV_BYTES;       // G x P tile
+  float* sW = reinterpret_cast<float*>(sP + G * Cfg::P_BYTES);  // a0, a1, b0, b1 [D]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sW + 4 * D);
+  uint64_t* bar_full = bars;       // [2] K/V stage loaded
+  uint64_t* bar_q = bars + 2;      // Q loaded
+  uint64_t* bar_mma = bars + 3;    // tcgen05.commit
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int unit = blockIdx.x;                        // b * H_kv + kh
+  const int n_mt = gridDim.y;
+  const int mt = n_mt - 1 - (int)blockIdx.y;          // longest tiles first
+  const int b = unit / p.H_kv, kh = unit % p.H_kv;
+  const int m0 = mt * BM;
+  const int S = p.S;
+  const int kv_end = min(m0 + BM, S);
+  const int ntiles = (kv_end + BN - 1) / BN;
+  const int H_q = p.H_kv * G;
+
+  auto stage_k = [&](int s, int src) { return sKV + (size_t)(s * 2 * NSRC + src) * Cfg::KV_BYTES; };
+  auto stage_v = [&](int s, int src) {
+    return sKV + (size_t)(s * 2 * NSRC + NSRC + src) * Cfg::KV_BYTES;
+  };
+
+  if (tid == 0) {
+    mbar_init(&bar_full[0], 1);
+    mbar_init(&bar_full[1], 1);
+    mbar_init(bar_q, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (NSRC == 2) {
+    for (int i = tid; i < D; i += NT) {
+      sW[i] = p.a0[kh * D + i];
+      sW[D + i] = p.a1[kh * D + i];
+      sW[2 * D + i] = p.b0[kh * D + i];
+      sW[3 * D + i] = p.b1[kh * D + i];
+    }
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto load_tile = [&](int j) {
+    const int s = j & 1;
+    const int n0 = j * BN;
+    mbar_arrive_expect_tx(&bar_full[s], 2 * NSRC * Cfg::KV_BYTES);
+    for (int cb = 0; cb < CB; ++cb) {
+      tma_load_3d(stage_k(s, 0) + cb * BN * SW, &maps.k0, cb * SWE, n0, unit, &bar_full[s]);
+      tma_load_3d(stage_v(s, 0) + cb * BN * SW, &maps.v0, cb * SWE, n0, unit, &bar_full[s]);
+      if (NSRC == 2) {
+        tma_load_3d(stage_k(s, 1) + cb * BN * SW, &maps.k1, cb * SWE, n0, unit, &bar_full[s]);
+        tma_load_3d(stage_v(s, 1) + cb * BN * SW, &maps.v1, cb * SWE, n0, unit, &bar_full[s]);
+      }
+    }
+  };
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_q, G * Cfg::Q_BYTES);
+    for (int h = 0; h < G; ++h)
+      for (int cb = 0; cb < CB; ++cb)
+        tma_load_3d(sQ + h * Cfg::Q_BYTES + cb * BM * SW, &maps.q, cb * SWE, m0,
+                    b * H_q + kh * G + h, bar_q);
+    load_tile(0);
+    if (ntiles > 1) load_tile(1);
+  }
+
+  // softmax state: thread owns query row `row` of head `hh`
+  const int hh = warp >> 2;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const int qpos = m0 + row;
+  const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+  const uint32_t t_s = tmem + lane_addr + hh * HEAD_COLS;
+  const uint32_t t_o = t_s + BN;
+  float m_run = -FLT_MAX, l_run = 0.f;
+  uint32_t mma_phase = 0;
+  bool failed = false;
+
+  constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
+  constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, true);
+
+  {
+    bool bad = !mbar_wait_bounded(bar_q, 0);
+    if (__syncthreads_or(bad)) failed = true;
+  }
+
+  for (int j = 0; j < ntiles && !failed; ++j) {
+    const int s = j & 1;
+    const int n0 = j * BN;
+    {
+      bool bad = !mbar_wait_bounded(&bar_full[s], (uint32_t)(j >> 1) & 1u);
+      if (__syncthreads_or(bad)) { failed = true; break; }
+    }
+    if (NSRC == 2) {
+      // K = a0 (.) K0 + a1 (.) K1 and V = b0 (.) V0 + b1 (.) V1, fp32 -> bf16,
+      // written over source 0 in the same swizzled layout.
+      constexpr int CHUNKS = CB * BN * (SW / 16);
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {
+        uint8_t* d0 = t == 0 ? stage_k(s, 0) : stage_v(s, 0);
+        const uint8_t* d1 = t == 0 ? stage_k(s, 1) : stage_v(s, 1);
+        const float* w0 = sW + (t == 0 ? 0 : 2 * D);
+        const float* w1 = sW + (t == 0 ? D : 3 * D);
+        for (int c = tid; c < CHUNKS; c += NT) {
+          const int cb = c / (BN * 4);
+          const int r = (c / 4) % BN;
+          const int pc = c & 3;
+          const int lc = pc ^ ((r >> 1) & 3);
+          const int col = cb * SWE + lc * 8;
+          uint4* p0 = reinterpret_cast<uint4*>(d0 + (size_t)c * 16);
+          const uint4 x = *p0;
+          const uint4 y = *reinterpret_cast<const uint4*>(d1 + (size_t)c * 16);
+          if (col >= D) continue;  // padding columns stay zero
+          float fx[8], fy[8];
+          unpack16<__nv_bfloat16>(x, fx);
+          unpack16<__nv_bfloat16>(y, fy);
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = w0[col + 2 * e] * fx[2 * e] + w1[col + 2 * e] * fy[2 * e];
+            const float hi = w0[col + 2 * e + 1] * fx[2 * e + 1] + w1[col + 2 * e + 1] * fy[2 * e + 1];
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(lo, hi);
+            o[e] = *reinterpret_cast<uint32_t*>(&v2);
+          }
+          *p0 = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+    }
+
+    // S_h = Q_h K^T for every head
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t kbase = smem_u32(stage_k(s, 0));
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const uint32_t qbase = smem_u32(sQ + h * Cfg::Q_BYTES);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (uint32_t)(k & 1) * 32;
+          const uint64_t ad = sdesc(qbase + (k >> 1) * BM * SW + off, 16, 8 * SW);
+          const uint64_t bd = sdesc(kbase + (k >> 1) * BN * SW + off, 16, 8 * SW);
+          mma_bf16(tmem + h * HEAD_COLS, ad, bd, IDESC_QK, k > 0);
+        }
+      }
+      mma_commit(bar_mma);
+    }
+    {
+      bool bad = !mbar_wait_bounded(bar_mma, mma_phase);
+      mma_phase ^= 1u;
+      if (__syncthreads_or(bad)) { failed = true; break; }
+    }
+    tc_fence_after();
+
+    // Online softmax of this thread's row.
+    float sv[BN];
+#pragma unroll
+    for (int c = 0; c < BN; c += 16) tmem_ld16(t_s + c, sv + c);
+    tmem_wait_ld();
+    float mt_row = -FLT_MAX;
+#pragma unroll
+    for (int c = 0; c < BN; ++c) {
+      const int kp = n0 + c;
+      const bool ok = kp <= qpos && kp < S;
+      sv[c] = ok ? sv[c] * p.scale_log2 : -FLT_MAX;
+      mt_row = fmaxf(mt_row, sv[c]);
+    }
+    const float m_new = fmaxf(m_run, mt_row);
+    const float alpha = fast_exp2(m_run - m_new);
+    float psum = 0.f;
+    uint8_t* prow = sP + hh * Cfg::P_BYTES;
+#pragma unroll
+    for (int c = 0; c < BN; c += 8) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = sv[c + 2 * e] == -FLT_MAX ? 0.f : fast_exp2(sv[c + 2 * e] - m_new);
+        const float x1 = sv[c + 2 * e + 1] == -FLT_MAX ? 0.f : fast_exp2(sv[c + 2 * e + 1] - m_new);
+        psum += x0 + x1;
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(x0, x1);
+        pk[e] = *reinterpret_cast<uint32_t*>(&v2);
+      }
+      const int blk = c / SWE, lc = (c % SWE) / 8;
+      *reinterpret_cast<uint4*>(prow + blk * BM * SW + swz64(row, lc)) =
+          make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+    if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll
+      for (int c = 0; c < D; c += 16) {
+        float ov[16];
+        tmem_ld16(t_o + c, ov);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ov[e] *= alpha;
+        tmem_st16(t_o + c, ov);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // O_h += P_h V
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t vbase = smem_u32(stage_v(s, 0));
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const uint32_t pbase = smem_u32(sP + h * Cfg::P_BYTES);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t ad = sdesc(pbase + (k >> 1) * BM * SW + (k & 1) * 32, 16, 8 * SW);
+          const uint64_t bd = sdesc(vbase + k * 16 * SW, BN * SW, 8 * SW);
+          mma_bf16(tmem + h * HEAD_COLS + BN, ad, bd, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(bar_mma);
+    }
+    {
+      bool bad = !mbar_wait_bounded(bar_mma, mma_phase);
+      mma_phase ^= 1u;
+      if (__syncthreads_or(bad)) { failed = true; break; }
+    }
+    tc_fence_after();
+    // stage s is free again: prefetch tile j + 2 into it
+    if (tid == 0 && j + 2 < ntiles) {
+      fence_proxy_async_smem();
+      load_tile(j + 2);
+    }
+  }
+
+  if (failed) {
+    if (tid == 0) flag_status(p.status, kDevTimeout);
+  } else {
+    // Epilogue: O_h / l -> bf16 rows of out[b, kh*G + hh, m0 + row, :].
+    const float inv = 1.f / l_run;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                          (((size_t)b * H_q + kh * G + hh) * S + qpos) * D;
+#pragma unroll
+    for (int c = 0; c < D; c += 16) {
+      float ov[16];
+      tmem_ld16(t_o + c, ov);
+      tmem_wait_ld();
+      uint32_t pk[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(ov[2 * e] * inv, ov[2 * e + 1] * inv);
+        pk[e] = *reinterpret_cast<uint32_t*>(&v2);
+      }
+      if (qpos < S) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// --- host side ---------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3-D bf16 map over rows of D elements: dims {D, rows, planes}, row stride
+// D*2 bytes, plane stride `plane_bytes`; box {32, box_rows, 1}, 64-byte swizzle.
+// Rows at or beyond `rows` read as zero.
+bool make_map(CUtensorMap* m, const void* base, int D, int rows, long long planes,
+              size_t plane_bytes, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)plane_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)SWE, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, int NSRC, int G>
+cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
+  PrefillMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const long long units = (long long)a.batch * a.kv_heads;
+  const size_t kv_plane = (size_t)a.max_seq * D * 2;
+  bool ok = make_map(&maps.q, a.q, D, a.S, (long long)a.batch * a.kv_heads * G,
+                     (size_t)a.S * D * 2, BM);
+  ok = ok && make_map(&maps.k0, a.k[0], D, a.S, units, kv_plane, BN);
+  ok = ok && make_map(&maps.v0, a.v[0], D, a.S, units, kv_plane, BN);
+  if (NSRC == 2) {
+    ok = ok && make_map(&maps.k1, a.k[1], D, a.S, units, kv_plane, BN);
+    ok = ok && make_map(&maps.v1, a.v[1], D, a.S, units, kv_plane, BN);
+  } else {
+    maps.k1 = maps.k0;
+    maps.v1 = maps.v0;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  PrefillParams p;
+  p.a0 = a.a[0];
+  p.a1 = a.a[1];
+  p.b0 = a.b[0];
+  p.b1 = a.b[1];
+  p.out = a.out;
+  p.status = a.status;
+  p.B = a.batch;
+  p.H_kv = a.kv_heads;
+  p.S = a.S;
+  p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+  const size_t smem = prefill_smem_bytes<D, NSRC, G>();
+  auto kern = prefill_kernel<D, NSRC, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)units, (unsigned)((a.S + BM - 1) / BM));
+  kern<<<grid, 128 * G, smem, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t by_src(const PrefillArgs& a, cudaStream_t s) {
+  if (a.group == 1) return a.nsrc == 2 ? launch_t<D, 2, 1>(a, s) : launch_t<D, 1, 1>(a, s);
+  if (a.group == 2) return a.nsrc == 2 ? launch_t<D, 2, 2>(a, s) : launch_t<D, 1, 2>(a, s);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t stream) {
+  if (a.batch * (long long)a.kv_heads > 65535 || a.S < 1) return cudaErrorNotSupported;
+  switch (a.head_dim) {
+    case 64: return by_src<64>(a, stream);
+    case 80: return by_src<80>(a, stream);
+    case 96: return by_src<96>(a, stream);
+    case 128: return by_src<128>(a, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace fkv

@@ -1,0 +1,144 @@
+"""GPU parity of fkv_prefill_attn (causal, tcgen05 tensor cores) against the
+float64 oracle, through the C ABI.  bf16 bars: max-abs 2e-2, rel-L2 5e-3."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from cross_layer_kv_gb300 import fusedkv as B
+from cross_layer_kv_gb300 import synth
+from parity import assert_close, f64
+
+pytestmark = pytest.mark.gpu
+
+MODES = ("vanilla", "lite", "fused")
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    yield
+    torch.cuda.synchronize()
+
+
+class PrefillSetup:
+    def __init__(self, w, layer, mode, S, seed=0, tie_keys=True):
+        self.w, self.layer, self.mode, self.S = w, layer, mode, S
+        n = w.n
+        need = [layer] if (layer <= n or mode == "vanilla") else sorted({1, n})
+        self.ctx = B.Context(w.num_layers, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim,
+                             "bf16", store_upper=any(l > n for l in need))
+        self.caches = {}
+        for l in need:
+            k, v = synth.make_cache(w, l, seed, "cuda")
+            self.caches[l] = (k, v)
+            self.ctx.fkv_bind_layer_cache(l, k, v)
+        self.weights = None
+        if layer > n:
+            self.weights = synth.make_weights(w, layer, seed, "cuda", tie_keys=tie_keys)
+            self.ctx.fkv_set_fusion_weights(layer, *self.weights)
+        g = torch.Generator(device="cuda").manual_seed(seed + 99)
+        self.q = torch.randn(w.batch, w.q_heads, S, w.head_dim, generator=g,
+                             device="cuda").to(torch.bfloat16)
+        self.out = torch.full_like(self.q, float("nan"))
+
+    def run(self):
+        self.ctx.fkv_prefill_attn(self.q, self.layer, self.mode, self.S, self.out)
+        return self.out
+
+    def oracle(self, bh=None, rows=None):
+        w = self.w
+        G = w.group
+        ws = ({self.layer: tuple(f64(x) for x in self.weights)} if self.weights else None)
+        if bh is None:
+            kc = {l: f64(k) for l, (k, v) in self.caches.items()}
+            vc = {l: f64(v) for l, (k, v) in self.caches.items()}
+            return O.prefill_attn(f64(self.q), self.layer, w.num_layers, self.mode, kc, vc,
+                                  weights=ws, rows=rows)
+        b, h = bh
+        kh = h // G
+        kc = {l: f64(k[b:b + 1, kh:kh + 1, :self.S]) for l, (k, v) in self.caches.items()}
+        vc = {l: f64(v[b:b + 1, kh:kh + 1, :self.S]) for l, (k, v) in self.caches.items()}
+        if ws:
+            ws = {self.layer: tuple(x[kh:kh + 1] for x in ws[self.layer])}
+        return O.prefill_attn(f64(self.q[b:b + 1, h:h + 1]), self.layer, w.num_layers, self.mode,
+                              kc, vc, weights=ws, rows=rows)[0, 0]
+
+    def close(self):
+        self.ctx.close()
+
+
+def _w(D, G, S_max, Bt=2, L=4):
+    return synth.Workload("p", L, Bt, S_max, 2 * G, 2, D, "bf16")
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("D", [64, 80, 96, 128])
+def test_prefill_small(mode, D):
+    w = _w(D, 2, 320)
+    s = PrefillSetup(w, 4, mode, 300, seed=1)
+    got = f64(s.run())
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    assert_close(got, s.oracle(), "bf16", "prefill D=%d %s" % (D, mode))
+    s.close()
+
+
+@pytest.mark.parametrize("S", [1, 2, 63, 64, 65, 128, 129, 256])
+def test_prefill_lengths_fused(S):
+    w = _w(96, 2, 256)
+    s = PrefillSetup(w, 3, "fused", S, seed=2)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "S=%d" % S)
+    s.close()
+
+
+@pytest.mark.parametrize("mode", ["lite", "fused"])
+def test_prefill_group_one(mode):
+    w = _w(64, 1, 200)
+    s = PrefillSetup(w, 3, mode, 200, seed=3)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "G=1 %s" % mode)
+    s.close()
+
+
+def test_prefill_storage_layer_and_untied():
+    w = _w(128, 2, 190)
+    s = PrefillSetup(w, 1, "fused", 190, seed=4)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "storage layer")
+    s.close()
+    s = PrefillSetup(w, 3, "fused", 190, seed=5, tie_keys=False)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "untied")
+    s.close()
+
+
+def test_prefill_rejects():
+    w = _w(64, 2, 64)
+    s = PrefillSetup(w, 3, "fused", 64)
+    with pytest.raises(B.FkvError) as e:   # S > S_max, checked by the library
+        s.ctx.fkv_prefill_attn(s.q.data_ptr(), 3, "fused", 65, s.out.data_ptr())
+    assert e.value.status == B.FKV_ERR_INVALID_ARG
+    with pytest.raises(B.FkvError) as e:
+        s.ctx.fkv_prefill_attn(s.q, 3, "vanilla", 64, s.out)
+    assert e.value.status == B.FKV_ERR_UNSUPPORTED
+    s.close()
+    ctx = B.Context(4, 1, 64, 2, 1, 64, "f32")
+    q = torch.zeros(1, 2, 8, 64, device="cuda")
+    with pytest.raises(B.FkvError) as e:
+        ctx.fkv_prefill_attn(q, 1, "vanilla", 8, q.clone())
+    assert e.value.status in (B.FKV_ERR_UNSUPPORTED, B.FKV_ERR_INVALID_ARG)
+    ctx.close()
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_prefill_full_size_sampled(mode):
+    """650M-shaped workload (B=4, S=8192, 16/8 heads, D=96): sampled rows."""
+    w = synth.M650_PREFILL
+    s = PrefillSetup(w, w.num_layers, mode, w.seq, seed=0)
+    got = f64(s.run())
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    rows = [0, 1, 127, 128, 129, 4095, 8190, 8191]
+    for b, h in [(0, 0), (3, 15), (1, 6), (2, 9)]:
+        ref = s.oracle((b, h), rows=rows)
+        assert_close(got[b, h, rows], ref, "bf16", "650M %s b=%d h=%d" % (mode, b, h))
+    s.close()
+    torch.cuda.empty_cache()
