@@ -70,6 +70,7 @@ _SIGS = {
     "fkv_decode_workspace_bytes": (ctypes.c_size_t, [_P]),
     "fkv_decode_attn": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, _P, _P, _P,
                                        ctypes.c_size_t, _P]),
+    "fkv_decode_attn_noalloc": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, _P, _P, _P]),
     "fkv_prefill_attn": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P]),
     "fkv_get_device_status": (ctypes.c_int, [_P, _P]),
     "fkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -230,6 +231,20 @@ class Context:
         _check(self._lib.fkv_decode_attn(self.handle, _ptr(q), layer, m, _ptr(seq_lens), _ptr(out),
                                          _ptr(workspace), nbytes, _stream(stream)),
                "fkv_decode_attn")
+        return out
+
+    def fkv_decode_attn_noalloc(self, q, layer: int, mode, seq_lens, out, stream=None):
+        """fkv_decode_attn for callers that cannot allocate: the partials live
+        in the library's own 4 MiB of static device memory."""
+        c = self.cfg
+        shape = (c.batch, c.num_q_heads, c.head_dim)
+        self._need(q, shape, self.torch_dtype, "q")
+        self._need(out, shape, self.torch_dtype, "out")
+        self._need(seq_lens, (c.batch,), torch.int32, "seq_lens")
+        m = MODES[mode] if isinstance(mode, str) else int(mode)
+        _check(self._lib.fkv_decode_attn_noalloc(self.handle, _ptr(q), layer, m, _ptr(seq_lens),
+                                                 _ptr(out), _stream(stream)),
+               "fkv_decode_attn_noalloc")
         return out
 
     def fkv_prefill_attn(self, q, layer: int, mode, S: int, out, stream=None):

@@ -135,6 +135,28 @@ fkv_status fkv_decode_attn(fkv_ctx* ctx, const void* q, int layer, int mode,
                            const int32_t* seq_lens, void* out, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* fkv_decode_attn without a caller workspace.  The paper has no counterpart:
+ * this is a deployment convenience of this library.
+ *
+ * It serves callers that cannot allocate device memory: a host process whose
+ * device memory is fully reserved by its own pool allocator, or a plugin
+ * interface that passes only the operands of one operation.  cudaMalloc is no
+ * way out for them, since it synchronises the device and fails once memory is
+ * exhausted.  This call runs the same kernels as fkv_decode_attn, with the
+ * split partials in a 4 MiB array that the library holds in static device
+ * memory on every GPU that loads it, until the process exits.  It calls no
+ * allocator.
+ *
+ * Arguments and results are those of fkv_decode_attn without workspace and
+ * workspace_bytes.  A context whose fkv_decode_workspace_bytes() exceeds
+ * 4 MiB gets FKV_ERR_WORKSPACE and nothing is launched.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All calls
+ * share the one array, and nothing in it needs to start at zero.  Calls whose
+ * kernels overlap on the GPU (e.g. on unordered streams) race on it. */
+fkv_status fkv_decode_attn_noalloc(fkv_ctx* ctx, const void* q, int layer, int mode,
+                                   const int32_t* seq_lens, void* out, void* stream);
+
 /* Causal prefill attention of a layer over a prompt occupying cache rows
  * [0, S) of every sequence (the storage caches already hold those rows).
  * q: device [B, H_q, S, D]; out: device [B, H_q, S, D]; context dtype.
