@@ -47,7 +47,7 @@ HBM_REF_GBS = 8000.0
 # DRAM traffic (read + write bytes per launch) of the fused split kernel on
 # this workload, from one ncu capture, and the source hash of the kernel it was
 # taken on; reported only while the kernel is unchanged.
-NCU_TRAFFIC = {"bytes_per_launch": None, "kernel_sha": None,
+NCU_TRAFFIC = {"bytes_per_launch": 1074042 * 1000 + 3229952, "kernel_sha": "a64fed8a884858f6",
                "profile": "profiles/decode_split_fused_332M.md"}
 
 
@@ -414,7 +414,7 @@ def main():
     traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["kernel_sha"] == _kernel_sha() else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": "fused upper-layer fkv_decode_attn (split + merge)",
+                "kernel": "fused upper-layer fkv_decode_attn (decode_split_kernel, in-kernel merge)",
                 "algorithmic_bytes_per_launch": call_bytes, "avg_launch_us": upper_ms * 1e3,
                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)"}
 

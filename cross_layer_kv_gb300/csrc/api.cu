@@ -1,6 +1,7 @@
 // The C ABI of include/fusedkv.h: context, host-side validation and dispatch
 // to the kernels.  Every check runs before any launch; nothing here allocates
 // on the hot path.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <new>
@@ -24,6 +25,10 @@ struct fkv_ctx {
 };
 
 namespace {
+
+// Process-wide call counter: tags each decode call's per-unit arrival counts
+// so that counts left in a reused workspace by earlier calls never match.
+std::atomic<unsigned> g_decode_epoch{1};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -215,6 +220,9 @@ fkv_status fkv_decode_attn(fkv_ctx* c, const void* q, int layer, int mode,
   d.out = out;
   d.seq_lens = seq_lens;
   d.workspace = static_cast<float*>(workspace);
+  unsigned ep = g_decode_epoch.fetch_add(1);
+  if (ep == 0) ep = g_decode_epoch.fetch_add(1);
+  d.epoch = ep;
   return fkv::decode_launch(d, plan, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FKV_OK
              : FKV_ERR_CUDA;

@@ -29,17 +29,27 @@ cudaError_t decode_launch_f32(const DecodeArgs& a, const DecodePlan& pl, cudaStr
   }
 }
 
-template <int D>
-static size_t smem_by_src(int nsrc, int B) {
-  return nsrc == 2 ? decode_smem_bytes<float, D, 2, 1>(B) : decode_smem_bytes<float, D, 1, 1>(B);
+template <int D, int NSRC>
+static size_t shape_by_group(int G, int B, int* warps) {
+  switch (G) {
+    case 1: *warps = DecodeShape<float, D, NSRC, 1>::W; return decode_smem_bytes<float, D, NSRC, 1>(B);
+    case 2: *warps = DecodeShape<float, D, NSRC, 2>::W; return decode_smem_bytes<float, D, NSRC, 2>(B);
+    case 4: *warps = DecodeShape<float, D, NSRC, 4>::W; return decode_smem_bytes<float, D, NSRC, 4>(B);
+    default: return 0;
+  }
 }
 
-size_t decode_smem_f32(int head_dim, int nsrc, int B) {
+template <int D>
+static size_t shape_by_src(int nsrc, int G, int B, int* warps) {
+  return nsrc == 2 ? shape_by_group<D, 2>(G, B, warps) : shape_by_group<D, 1>(G, B, warps);
+}
+
+size_t decode_shape_f32(int head_dim, int nsrc, int G, int B, int* warps) {
   switch (head_dim) {
-    case 64: return smem_by_src<64>(nsrc, B);
-    case 80: return smem_by_src<80>(nsrc, B);
-    case 96: return smem_by_src<96>(nsrc, B);
-    case 128: return smem_by_src<128>(nsrc, B);
+    case 64: return shape_by_src<64>(nsrc, G, B, warps);
+    case 80: return shape_by_src<80>(nsrc, G, B, warps);
+    case 96: return shape_by_src<96>(nsrc, G, B, warps);
+    case 128: return shape_by_src<128>(nsrc, G, B, warps);
     default: return 0;
   }
 }

@@ -29,8 +29,13 @@
 //    sources and b is applied once when the partial is written.  Nothing
 //    reconstructed is written to memory.
 //  * All G query heads of a KV head share each tile read (GQA reuse); online
-//    softmax in base 2 with warp-shuffle reductions; a second kernel merges
-//    the partials of each (b, h) with their log-sum-exp weights.
+//    softmax in base 2 with warp-shuffle reductions.
+//  * The warp that writes the last partial of a (b, kh) unit merges the
+//    unit's partials with their log-sum-exp weights and writes the output
+//    rows, so one call is one kernel.  Arrivals are counted per unit in a
+//    64-bit word tagged with the call's epoch: a count left by an earlier call
+//    (or by a call that stopped early) carries another epoch and restarts, so
+//    the workspace never needs clearing.
 #pragma once
 
 #include <cfloat>
@@ -41,24 +46,67 @@
 
 namespace fkv {
 
-template <typename T, int D, int NSRC>
+// Launch shape of the decode kernel per element type, head dim, source count
+// and group size: W warps per CTA, NS ring stages per warp, SB bytes per stage,
+// VEC 16-byte chunks per lane.  Chosen from launch-shape sweeps on GB300 at the
+// 332M (D=64), 4B (D=80) and 1.5B (D=128) workloads:
+//  * power-of-two rows (128 / 256 bytes): 8 warps; one source streams best
+//    from 2 x 12 KB stages, two sources from 3 x 8 KB;
+//  * 160 / 192-byte rows (D = 80, 96): 2 chunks per lane (5 or 6 lanes per
+//    row instead of 10 or 12, so 2.5x fewer shuffles per row); one source
+//    with 16 warps x 2 x 6 KB, two sources with 8 warps x 2 x 12 KB (their
+//    registers do not fit the 128 a thread gets at 16 warps);
+//  * G = 4 or fp32 rows wider than 256 bytes: 8 warps x 3 x 8 KB, 1 chunk.
+// Every shape keeps 96-192 KB of loads in flight per SM.
+// FKV_DECODE_{WARPS,STAGES,STAGE_BYTES,VEC} override all shapes at build time
+// (for tuning sweeps).
+template <typename T, int D, int NSRC, int G>
+struct DecodeShape {
+  static constexpr int ROWB = D * (int)sizeof(T);
+  static constexpr bool pow2 = ROWB == 128 || ROWB == 256;
+  static constexpr bool odd = (ROWB == 160 || ROWB == 192) && G <= 2;
+  static constexpr int W0 = odd && NSRC == 1 ? 16 : 8;
+  static constexpr int NS0 = (pow2 && NSRC == 2) || (!pow2 && !odd) ? 3 : 2;
+  static constexpr int SB0 = NS0 == 3 ? 8192 : (W0 == 16 ? 6144 : 12288);
+  static constexpr int VEC0 = odd ? 2 : 1;
+#ifdef FKV_DECODE_WARPS
+  static constexpr int W = FKV_DECODE_WARPS;
+#else
+  static constexpr int W = W0;
+#endif
+#ifdef FKV_DECODE_STAGES
+  static constexpr int NS = FKV_DECODE_STAGES;
+#else
+  static constexpr int NS = NS0;
+#endif
+#ifdef FKV_DECODE_STAGE_BYTES
+  static constexpr int SB = FKV_DECODE_STAGE_BYTES;
+#else
+  static constexpr int SB = SB0;
+#endif
+#ifdef FKV_DECODE_VEC
+  static constexpr int VEC = ROWB % (16 * FKV_DECODE_VEC) == 0 ? FKV_DECODE_VEC : 1;
+#else
+  static constexpr int VEC = VEC0;
+#endif
+};
+
+template <typename T, int D, int NSRC, int SB, int VEC>
 struct DecodeCfg {
   static constexpr int ROWB = D * (int)sizeof(T);   // bytes per cache row
-  static constexpr int C = ROWB / 16;                // 16-byte chunks per row
+  static constexpr int C = ROWB / (16 * VEC);        // lanes per row (VEC 16-byte chunks each)
   static constexpr int R = 32 / C;                   // rows per warp step
-  static constexpr int E = 16 / (int)sizeof(T);      // elements per chunk
-  static constexpr int STAGE_TARGET = 8192;          // bytes per stage (all tensors)
+  static constexpr int EC = 16 / (int)sizeof(T);     // elements per 16-byte chunk
+  static constexpr int E = EC * VEC;                 // elements per lane
+  static constexpr int STAGE_TARGET = SB;             // bytes per stage (all tensors)
   static constexpr int STEPS_RAW = STAGE_TARGET / (2 * NSRC * R * ROWB);
   static constexpr int STEPS = STEPS_RAW < 1 ? 1 : STEPS_RAW;
   static constexpr int TR = R * STEPS;               // rows per tile
   static constexpr int TILE_BYTES = TR * ROWB;       // one tensor's tile
   static constexpr int STAGE_BYTES = 2 * NSRC * TILE_BYTES;
-  static_assert(ROWB % 16 == 0, "row must be a multiple of 16 bytes");
+  static_assert(ROWB % (16 * VEC) == 0, "row must split into whole lane chunks");
   static_assert(C >= 1 && C <= 32, "row must fit one warp of 16-byte chunks");
 };
-
-constexpr int kDecodeWarps = 8;    // warps per CTA
-constexpr int kDecodeStages = 3;   // pipeline stages per warp
 
 // Partial record of one (slot, query head): o[D] then m, l (padded to 4).
 __host__ __device__ constexpr int partial_stride(int D) { return D + 4; }
@@ -73,20 +121,14 @@ struct SplitParams {
   const float* b0;
   const float* b1;
   const void* q;
+  void* out;
   const int32_t* seq_lens;
-  float* ws;
+  float* ws;                       // partials
+  unsigned long long* counters;    // one arrival word per (b, kh) unit
   int* status;
   int B, H_kv, S_max;
+  unsigned epoch;                  // tag of this call's arrivals
   float qscale;  // softmax scale * log2(e)
-};
-
-struct MergeParams {
-  const int32_t* seq_lens;
-  const float* ws;
-  void* out;
-  int B, H_kv, G, S_max, D;
-  int total_warps;
-  int is_f32;
 };
 
 // Walk of a warp's row range, one tile at a time, crossing (b, kh) units.
@@ -119,6 +161,26 @@ struct RowWalker {
   }
 };
 
+// VEC consecutive 16-byte chunks of shared memory -> fp32.
+template <typename T, int VEC>
+__device__ __forceinline__ void load_chunks(const uint8_t* src, float* f) {
+#pragma unroll
+  for (int v = 0; v < VEC; ++v)
+    unpack16<T>(*reinterpret_cast<const uint4*>(src + 16 * v), f + v * (16 / (int)sizeof(T)));
+}
+
+// (c0, c1) += (a0, a1) * (b0, b1) with one packed fp32 FMA (fma.rn.f32x2).
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 A, B, C;\n\t"
+      "mov.b64 A, {%2, %3};\n\t"
+      "mov.b64 B, {%4, %5};\n\t"
+      "mov.b64 C, {%0, %1};\n\t"
+      "fma.rn.f32x2 C, A, B, C;\n\t"
+      "mov.b64 {%0, %1}, C;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Sum over the C lanes of each row group; every lane of the group gets it.
 template <int C>
 __device__ __forceinline__ float group_sum(float v, int lane) {
@@ -143,18 +205,96 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Count one arrival on a unit's word for call `epoch`; returns the count of
+// this epoch including this arrival (0 if the retry bound ran out).  A word
+// holding another epoch restarts at 1.
+__device__ __forceinline__ unsigned unit_arrive(unsigned long long* word, unsigned epoch) {
+  unsigned long long old = atomicAdd(word, 0ull);
+#pragma unroll 1
+  for (int i = 0; i < (1 << 20); ++i) {
+    const unsigned long long nv = (unsigned)(old >> 32) == epoch
+                                      ? old + 1ull
+                                      : (((unsigned long long)epoch << 32) | 1ull);
+    const unsigned long long prev = atomicCAS(word, old, nv);
+    if (prev == old) return (unsigned)(nv & 0xffffffffull);
+    old = prev;
+  }
+  return 0;
+}
+
+// Merge the partials of unit (b, h) -- written by warps wf..wl, skipping the
+// ones with empty ranges -- into the G output rows.  One warp; partials are
+// read through L2 (__ldcg), since other SMs wrote them in this launch.
+template <typename T, int D, int G>
+__device__ __forceinline__ void merge_unit(const float* ws, T* out, long long u, long long wf,
+                                           long long wl, long long N, long long total, int b,
+                                           int h, int H, int lane) {
+  constexpr int PS = partial_stride(D);
+  constexpr int DPL = (D + 31) / 32;
+#pragma unroll 1
+  for (int hq = 0; hq < G; ++hq) {
+    float M = -FLT_MAX;
+    for (long long w0 = wf; w0 <= wl; w0 += 32) {
+      const long long w = w0 + lane;
+      if (w <= wl && w * total / N < (w + 1) * total / N)
+        M = fmaxf(M, __ldcg(ws + ((size_t)(w + u) * G + hq) * PS + D));
+    }
+    M = warp_max(M);
+    float L = 0.f;
+    float acc[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+    for (long long w0 = wf; w0 <= wl; w0 += 32) {
+      const long long w = w0 + lane;
+      float sc = 0.f;
+      if (w <= wl && w * total / N < (w + 1) * total / N) {
+        const float* rec = ws + ((size_t)(w + u) * G + hq) * PS;
+        sc = exp2f(__ldcg(rec + D) - M);
+        L += sc * __ldcg(rec + D + 1);
+      }
+      const int cnt = (int)min(32LL, wl - w0 + 1);
+#pragma unroll 1
+      for (int i = 0; i < cnt; ++i) {
+        const float si = __shfl_sync(0xffffffffu, sc, i);
+        if (si == 0.f) continue;
+        const float* rec = ws + ((size_t)(w0 + i + u) * G + hq) * PS;
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) {
+          const int d = lane + 32 * k;
+          if (d < D) acc[k] = fmaf(si, __ldcg(rec + d), acc[k]);
+        }
+      }
+    }
+    const float inv = 1.f / warp_sum(L);
+    T* orow = out + ((size_t)b * H * G + (size_t)h * G + hq) * D;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+      const int d = lane + 32 * k;
+      if (d < D) {
+        if constexpr (sizeof(T) == 4) orow[d] = acc[k] * inv;
+        else orow[d] = __float2bfloat16_rn(acc[k] * inv);
+      }
+    }
+  }
+}
+
 // Shared-memory bytes of the split kernel besides the stages.
 __host__ __device__ constexpr size_t decode_aux_bytes(int warps, int stages, int B) {
   return (size_t)warps * stages * 8 + (size_t)(2 * B + 2) * 4;
 }
 
-template <typename T, int D, int NSRC, int G>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 1)
-    decode_split_kernel(const SplitParams p) {
-  using Cfg = DecodeCfg<T, D, NSRC>;
+template <typename T, int D, int NSRC, int G, int W, int NS, int SB, int VEC>
+__global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitParams p) {
+  using Cfg = DecodeCfg<T, D, NSRC, SB, VEC>;
   constexpr int C = Cfg::C, R = Cfg::R, E = Cfg::E, TR = Cfg::TR, STEPS = Cfg::STEPS;
+  constexpr int EC = Cfg::EC;
   constexpr int ROWB = Cfg::ROWB, TILE = Cfg::TILE_BYTES, STAGE = Cfg::STAGE_BYTES;
-  constexpr int NS = kDecodeStages, W = kDecodeWarps;
   constexpr int PS = partial_stride(D);
 
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -201,6 +341,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   __syncthreads();
 
   const int H = p.H_kv;
+  if (blockIdx.x == 0) {
+    // sequences of length 0 have no rows and so no merging warp: zero output
+    const int row_elems = H * G * D;
+    for (int bb = 0; bb < p.B; ++bb) {
+      if (lens[bb] != 0) continue;
+      for (int i = threadIdx.x; i < row_elems; i += blockDim.x) {
+        const size_t o = (size_t)bb * row_elems + i;
+        if constexpr (sizeof(T) == 4) static_cast<float*>(p.out)[o] = 0.f;
+        else static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
+      }
+    }
+  }
   const long long total = (long long)H * pre[p.B];
   const long long N = (long long)gridDim.x * W;
   const long long w = (long long)blockIdx.x * W + warp;
@@ -291,7 +443,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
       for (int hq = 0; hq < G; ++hq) {
         float qf[E];
-        unpack16<T>(*reinterpret_cast<const uint4*>(qp + (size_t)hq * D), qf);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v)
+          unpack16<T>(*reinterpret_cast<const uint4*>(qp + (size_t)hq * D + v * EC), qf + v * EC);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           qa[hq][e] = qf[e] * p.qscale * wa0[e];
@@ -324,23 +478,27 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
     for (int j = 0; j < STEPS; ++j) {
       const int row = j * R + g;
-      float acc[G];
+      float acc[G], acc2[G];
 #pragma unroll
-      for (int hq = 0; hq < G; ++hq) acc[hq] = 0.f;
+      for (int hq = 0; hq < G; ++hq) acc[hq] = acc2[hq] = 0.f;
       if (active) {
         float kf[E];
-        unpack16<T>(*reinterpret_cast<const uint4*>(kt0 + row * ROWB + c * 16), kf);
+        load_chunks<T, VEC>(kt0 + row * ROWB + c * 16 * VEC, kf);
 #pragma unroll
         for (int hq = 0; hq < G; ++hq)
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[hq] = fmaf(qa[hq][e], kf[e], acc[hq]);
+          for (int e = 0; e < E; e += 2)
+            fma2(acc[hq], acc2[hq], qa[hq][e], qa[hq][e + 1], kf[e], kf[e + 1]);
         if constexpr (NSRC == 2) {
-          unpack16<T>(*reinterpret_cast<const uint4*>(kt1 + row * ROWB + c * 16), kf);
+          load_chunks<T, VEC>(kt1 + row * ROWB + c * 16 * VEC, kf);
 #pragma unroll
           for (int hq = 0; hq < G; ++hq)
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[hq] = fmaf(qb[hq][e], kf[e], acc[hq]);
+            for (int e = 0; e < E; e += 2)
+              fma2(acc[hq], acc2[hq], qb[hq][e], qb[hq][e + 1], kf[e], kf[e + 1]);
         }
+#pragma unroll
+        for (int hq = 0; hq < G; ++hq) acc[hq] += acc2[hq];
       }
       const bool ok = active && row < n;
 #pragma unroll
@@ -381,17 +539,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
           l[hq] += pj[hq];
         }
         float vf[E];
-        unpack16<T>(*reinterpret_cast<const uint4*>(vt0 + row * ROWB + c * 16), vf);
+        load_chunks<T, VEC>(vt0 + row * ROWB + c * 16 * VEC, vf);
 #pragma unroll
         for (int hq = 0; hq < G; ++hq)
 #pragma unroll
-          for (int e = 0; e < E; ++e) o0[hq][e] = fmaf(pj[hq], vf[e], o0[hq][e]);
+          for (int e = 0; e < E; e += 2)
+            fma2(o0[hq][e], o0[hq][e + 1], pj[hq], pj[hq], vf[e], vf[e + 1]);
         if constexpr (NSRC == 2) {
-          unpack16<T>(*reinterpret_cast<const uint4*>(vt1 + row * ROWB + c * 16), vf);
+          load_chunks<T, VEC>(vt1 + row * ROWB + c * 16 * VEC, vf);
 #pragma unroll
           for (int hq = 0; hq < G; ++hq)
 #pragma unroll
-            for (int e = 0; e < E; ++e) o1[hq][e] = fmaf(pj[hq], vf[e], o1[hq][e]);
+            for (int e = 0; e < E; e += 2)
+              fma2(o1[hq][e], o1[hq][e + 1], pj[hq], pj[hq], vf[e], vf[e + 1]);
         }
       }
     }
@@ -447,88 +607,36 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         }
       }
       fresh = true;
-    }
-  }
-}
 
-// Merge of the partials of each (b, query head): one warp per output row.
-template <typename T>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-  grid_dep_trigger();
-  grid_dep_wait();
-  const int Hq = p.H_kv * p.G;
-  if (row >= (long long)p.B * Hq) return;
-  const int b = (int)(row / Hq), hq = (int)(row % Hq);
-  const int h = hq / p.G, hl = hq % p.G;
-  const int D = p.D, PS = partial_stride(D);
-
-  auto clamp_len = [&](int L) { return L < 0 ? 0 : (L > p.S_max ? p.S_max : L); };
-  long long before = 0, total = 0;
-  for (int base = 0; base < p.B; base += 32) {
-    const int i = base + lane;
-    const long long L = i < p.B ? clamp_len(p.seq_lens[i]) : 0;
-    long long x = L, y = i < b ? L : 0;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      x += __shfl_xor_sync(0xffffffffu, x, o);
-      y += __shfl_xor_sync(0xffffffffu, y, o);
-    }
-    total += x;
-    before += y;
-  }
-  const int Lb = clamp_len(p.seq_lens[b]);
-  T* out = static_cast<T*>(p.out) + (size_t)row * D;
-  if (Lb == 0) {
-    for (int d = lane; d < D; d += 32) {
-      if constexpr (sizeof(T) == 4) out[d] = 0.f;
-      else out[d] = __float2bfloat16_rn(0.f);
-    }
-    return;
-  }
-  const long long H = p.H_kv, N = p.total_warps;
-  total *= H;
-  const long long su = H * before + (long long)h * Lb, eu = su + Lb;
-  const long long u = (long long)b * H + h;
-  const long long wf = ((su + 1) * N - 1) / total, wl = (eu * N - 1) / total;
-
-  float M = -FLT_MAX;
-  for (long long w = wf; w <= wl; ++w) {
-    const long long s0 = w * total / N, s1 = (w + 1) * total / N;
-    if (s0 >= s1 || s0 >= eu || s1 <= su) continue;
-    M = fmaxf(M, p.ws[((size_t)(w + u) * p.G + hl) * PS + D]);
-  }
-  float Lsum = 0.f;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // D <= 128
-  for (long long w = wf; w <= wl; ++w) {
-    const long long s0 = w * total / N, s1 = (w + 1) * total / N;
-    if (s0 >= s1 || s0 >= eu || s1 <= su) continue;
-    const float* rec = p.ws + ((size_t)(w + u) * p.G + hl) * PS;
-    const float sc = exp2f(rec[D] - M);
-    Lsum += sc * rec[D + 1];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int d = lane + 32 * k;
-      if (d < D) acc[k] += sc * rec[d];
-    }
-  }
-  const float inv = 1.f / Lsum;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int d = lane + 32 * k;
-    if (d < D) {
-      if constexpr (sizeof(T) == 4) out[d] = acc[k] * inv;
-      else out[d] = __float2bfloat16_rn(acc[k] * inv);
+      // Publish the partial, count the arrival; the last warp of the unit merges.
+      const long long su = (long long)H * pre[b] + (long long)h * lens[b];
+      const long long eu = su + lens[b];
+      const long long wf = ((su + 1) * N - 1) / total, wl = (eu * N - 1) / total;
+      int need = 0;
+      for (long long w0 = wf; w0 <= wl; w0 += 32) {
+        const long long ww = w0 + lane;
+        need += __popc(__ballot_sync(0xffffffffu,
+                                     ww <= wl && ww * total / N < (ww + 1) * total / N));
+      }
+      __threadfence();
+      __syncwarp();
+      unsigned arrived = 0;
+      if (lane == 0) arrived = unit_arrive(p.counters + u, p.epoch);
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      if (arrived == 0) flag_status(p.status, lane == 0 ? kDevTimeout : 0);
+      if (arrived == (unsigned)need) {
+        __threadfence();
+        merge_unit<T, D, G>(p.ws, static_cast<T*>(p.out), u, wf, wl, N, total, b, h, H, lane);
+      }
     }
   }
 }
 
 template <typename T, int D, int NSRC, int G>
 size_t decode_smem_bytes(int B) {
-  using Cfg = DecodeCfg<T, D, NSRC>;
-  return (size_t)kDecodeWarps * kDecodeStages * Cfg::STAGE_BYTES +
-         decode_aux_bytes(kDecodeWarps, kDecodeStages, B);
+  using S = DecodeShape<T, D, NSRC, G>;
+  using Cfg = DecodeCfg<T, D, NSRC, S::SB, S::VEC>;
+  return (size_t)S::W * S::NS * Cfg::STAGE_BYTES + decode_aux_bytes(S::W, S::NS, B);
 }
 
 template <typename T, int D, int NSRC, int G>
@@ -543,34 +651,23 @@ cudaError_t decode_launch_t(const DecodeArgs& a, const DecodePlan& plan, cudaStr
   sp.b0 = a.b[0];
   sp.b1 = a.b[1];
   sp.q = a.q;
+  sp.out = a.out;
   sp.seq_lens = a.seq_lens;
   sp.ws = a.workspace;
+  sp.counters = reinterpret_cast<unsigned long long*>(
+      reinterpret_cast<char*>(a.workspace) + plan.partial_bytes);
   sp.status = a.status;
+  sp.epoch = a.epoch;
   sp.B = a.batch;
   sp.H_kv = a.kv_heads;
   sp.S_max = a.max_seq;
   sp.qscale = a.softmax_scale * 1.4426950408889634f;
-  auto kern = decode_split_kernel<T, D, NSRC, G>;
+  using S = DecodeShape<T, D, NSRC, G>;
+  auto kern = decode_split_kernel<T, D, NSRC, G, S::W, S::NS, S::SB, S::VEC>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem_bytes);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(plan.ctas), dim3(kDecodeWarps * 32), plan.smem_bytes, stream, sp);
-  if (e != cudaSuccess) return e;
-
-  MergeParams mp;
-  mp.seq_lens = a.seq_lens;
-  mp.ws = a.workspace;
-  mp.out = a.out;
-  mp.B = a.batch;
-  mp.H_kv = a.kv_heads;
-  mp.G = G;
-  mp.S_max = a.max_seq;
-  mp.D = D;
-  mp.total_warps = plan.ctas * kDecodeWarps;
-  mp.is_f32 = sizeof(T) == 4;
-  const long long rows = (long long)a.batch * a.kv_heads * G;
-  return launch_pdl(decode_merge_kernel<T>, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, stream,
-                    mp);
+  return launch_pdl(kern, dim3(plan.ctas), dim3(S::W * 32), plan.smem_bytes, stream, sp);
 }
 
 }  // namespace fkv

@@ -26,6 +26,7 @@ struct DecodeArgs {
   int is_f32;
   float softmax_scale;
   int num_ctas;              // split grid (0 = library default)
+  unsigned epoch;            // distinct per call (tags the unit arrival counts)
 };
 
 // Launch configuration the library picks for a decode call shape.
@@ -33,17 +34,18 @@ struct DecodePlan {
   int ctas;          // CTAs of the split kernel
   int warps_per_cta;
   size_t smem_bytes;
+  size_t partial_bytes;    // split partials, then one 8-byte arrival word per unit
   size_t workspace_bytes;
 };
 
 // Plan (grid and workspace) for a shape; num_sms from the device.
 cudaError_t decode_plan(const DecodeArgs& a, int num_sms, DecodePlan* plan);
 
-// Launch split kernel + merge kernel on `stream`.
+// Launch the decode kernel on `stream`.
 cudaError_t decode_launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
 
 // Number of kernel launches one decode call makes (for launch accounting).
-constexpr int kDecodeLaunchesPerCall = 2;
+constexpr int kDecodeLaunchesPerCall = 1;
 
 // Launch `kern` with programmatic stream serialization (see grid_dep_wait).
 template <typename Kern, typename... Args>

@@ -29,8 +29,8 @@ FKV_VANILLA, FKV_LITE, FKV_FUSED = 0, 1, 2
 MODES = {"vanilla": FKV_VANILLA, "lite": FKV_LITE, "fused": FKV_FUSED}
 FKV_BF16, FKV_F32 = 0, 1
 
-# Kernel launches per call: decode = split kernel + merge kernel; append = 1.
-DECODE_LAUNCHES_PER_CALL = 2
+# Kernel launches per call: decode = 1 (split + in-kernel merge); append = 1.
+DECODE_LAUNCHES_PER_CALL = 1
 APPEND_LAUNCHES_PER_CALL = 1
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),

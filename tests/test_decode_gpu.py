@@ -174,3 +174,18 @@ def test_full_size_storage_layer():
     assert_close(np.stack([got[b, h] for b, h in pairs]), s.oracle("fused", pairs), "bf16",
                  "storage layer 1")
     s.close()
+
+
+def test_workspace_garbage_and_reuse():
+    """The workspace needs no clearing: random bytes in it, or counts left by
+    earlier calls of other shapes, do not change the result."""
+    w = _small(80, 2, S=900, Bt=4)
+    s = DecodeSetup(w, 5, ["fused", "lite"], seed=13, lens=[900, 17, 450, 1])
+    g = torch.Generator(device="cuda").manual_seed(5)
+    s.ws.copy_(torch.randint(0, 256, s.ws.shape, generator=g, device="cuda", dtype=torch.uint8))
+    ref_f, ref_l = s.oracle("fused"), s.oracle("lite")
+    for _ in range(3):
+        assert_close(f64(s.run("fused")), ref_f, "bf16", "fused, dirty workspace")
+        assert_close(f64(s.run("lite")), ref_l, "bf16", "lite, dirty workspace")
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    s.close()
