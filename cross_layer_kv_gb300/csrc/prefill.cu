@@ -10,21 +10,25 @@
 // global memory (Table 1 slide: fuse on demand; reading notes §2.3).
 //
 // Structure of one CTA: one 128-row query tile of one (b, kh) unit and all G
-// query heads of that KV head (one warpgroup per head).
-//  * TMA (cp.async.bulk.tensor, 64-byte swizzle) loads the Q tiles once and the
-//    K/V source tiles of 64 keys into a 2-stage ring; the loads of tile j+2
-//    overlap the work on tile j.
-//  * Fused mode: the warps combine the two sources of each K and V tile in
-//    fp32 and write the bf16 result in place, in the same swizzled layout the
-//    tensor cores read (the fused tile is shared by all G heads).
-//  * One thread issues tcgen05.mma: S_h = Q_h K^T into tensor memory, then,
-//    after the softmax warps have written P_h (bf16) to shared memory,
-//    O_h += P_h V, also accumulated in tensor memory.
-//  * Softmax: each thread owns one query row (one TMEM lane), reads its S row
-//    with tcgen05.ld, applies the causal mask and the online (base-2) softmax,
-//    rescales its O row in tensor memory when the running max grows.
-//  * Every wait is bounded; a wait that runs out flags the device status,
-//    releases the tensor memory and returns.
+// query heads of that KV head, with warps specialised by role:
+//  * a TMA producer warp (cp.async.bulk.tensor, 64-byte swizzle) loads the Q
+//    tiles once and the K/V source tiles of 64 keys into a ring of up to 4
+//    stages;
+//  * fused mode: a fusion warpgroup combines the two sources of each K and V
+//    tile in fp32 and writes the bf16 result in place, in the swizzled layout
+//    the tensor cores read (the fused tile serves all G heads);
+//  * an MMA warp issues tcgen05.mma: S_h = Q_h K^T into a double-buffered
+//    tensor-memory tile, and O_h += P_h V accumulated in tensor memory; the S
+//    of the next tile is issued before the P of this one is awaited, so the
+//    tensor cores work while the softmax warps run;
+//  * one softmax warpgroup per head: each thread owns one query row (one TMEM
+//    lane), reads its S row with tcgen05.ld, applies the causal mask and the
+//    online (base-2) softmax and writes P_h (bf16) to swizzled shared memory;
+//    O is rescaled in tensor memory only when the running max grows by more
+//    than 2^8.
+//  * Every wait is bounded; a wait that runs out sets an abort flag that
+//    every role checks, flags the device status, and the CTA releases its
+//    tensor memory and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -175,295 +179,360 @@ struct PrefillMaps {
   CUtensorMap k0, k1, v0, v1;
 };
 
+constexpr int SMEM_LIMIT = 232448;   // opt-in dynamic shared memory per CTA (227 KB)
+constexpr int AUX_BYTES = 512;       // barriers, TMEM slot, abort flag
+constexpr float RESCALE_SLACK = 8.f; // log2 growth of the running max tolerated before O is rescaled
+
+template <int D, int NSRC, int G>
+struct PrefillPlan {
+  using Cfg = PrefillCfg<D>;
+  static constexpr int STAGE = 2 * NSRC * Cfg::KV_BYTES;
+  static constexpr int FIXED = G * Cfg::Q_BYTES + G * Cfg::P_BYTES + 4 * D * 4 + AUX_BYTES + 512;
+  static constexpr int NS_FIT = (SMEM_LIMIT - FIXED) / STAGE;
+  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;   // K/V ring stages
+  static constexpr int SOFTMAX_WARPS = 4 * G;
+  static constexpr int FUSION_WARPS = NSRC == 2 ? 4 : 0;
+  static constexpr int PRODUCER_WARP = SOFTMAX_WARPS + FUSION_WARPS;
+  static constexpr int MMA_WARP = PRODUCER_WARP + 1;
+  static constexpr int THREADS = 32 * (MMA_WARP + 1);
+  static_assert(NS >= 2, "shared memory too small for two K/V stages");
+};
+
 template <int D, int NSRC, int G>
 size_t prefill_smem_bytes() {
-  using Cfg = PrefillCfg<D>;
-  size_t s = (size_t)G * Cfg::Q_BYTES + 2ull * 2 * NSRC * Cfg::KV_BYTES + (size_t)G * Cfg::P_BYTES;
-  s += 4 * D * sizeof(float);  // fusion weights
-  s += 64;                     // barriers + TMEM slot
-  s += 512;                    // alignment slack
+  using P = PrefillPlan<D, NSRC, G>;
+  size_t s = (size_t)P::FIXED + (size_t)P::NS * P::STAGE;
   // at least 116 KB so that one CTA holds an SM (it takes all 512 TMEM columns)
   return s < 118784 ? 118784 : s;
 }
 
+// Warp-specialised CTA (G query heads of one KV head, 128 query rows each):
+//   softmax warpgroups (one per head) | fusion warpgroup (fused mode) |
+//   TMA producer warp | MMA warp.
+// Pipeline per 64-key tile j, all hand-offs through mbarriers:
+//   producer:  kv_empty[s] -> TMA K/V sources -> kv_full[s]
+//   fusion:    kv_full[s] -> fused bf16 K/V written in place -> kv_ready[s]
+//   MMA:       kv_ready[s] -> S_h[j%2] = Q_h K^T -> s_full[h][j%2];
+//              p_full[h] -> O_h += P_h V -> o_done[h]; then -> kv_empty[s]
+//              (S of tile j+1 is issued before waiting for P of tile j)
+//   softmax h: s_full -> row max / exp -> (o_done of tile j-1) -> rescale O
+//              in TMEM if the max grew by more than 2^8 -> P_h -> p_full[h]
 template <int D, int NSRC, int G>
-__global__ void __launch_bounds__(128 * G, 1)
+__global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillParams p) {
   using Cfg = PrefillCfg<D>;
-  constexpr int CB = Cfg::CB;
-  constexpr int NT = 128 * G;
+  using PL = PrefillPlan<D, NSRC, G>;
+  constexpr int CB = Cfg::CB, NS = PL::NS;
   extern __shared__ uint8_t smem_raw[];
   // 512-byte alignment: the period of the 64-byte swizzle pattern
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 511) &
                                              ~uintptr_t(511));
-  uint8_t* sQ = smem;                                     // G x Q tile
-  uint8_t* sKV = sQ + G * Cfg::Q_BYTES;                   // 2 stages x (K srcs, V srcs)
-  uint8_t* sP = sKV + 2 * 2 * NSRC * Cfg::KV_BYTES;       // G x P tile
-  float* sW = reinterpret_cast<float*>(sP + G * Cfg::P_BYTES);  // a0, a1, b0, b1 [D]
+  uint8_t* sQ = smem;
+  uint8_t* sKV = sQ + G * Cfg::Q_BYTES;
+  uint8_t* sP = sKV + NS * PL::STAGE;
+  float* sW = reinterpret_cast<float*>(sP + G * Cfg::P_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sW + 4 * D);
-  uint64_t* bar_full = bars;       // [2] K/V stage loaded
-  uint64_t* bar_q = bars + 2;      // Q loaded
-  uint64_t* bar_mma = bars + 3;    // tcgen05.commit
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
+  uint64_t* bar_q = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_ready = kv_full + NS;
+  uint64_t* kv_empty = kv_ready + NS;
+  uint64_t* s_full = kv_empty + NS;     // [G][2]
+  uint64_t* p_full = s_full + 2 * G;    // [G]
+  uint64_t* o_done = p_full + G;        // [G]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + G);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.x;                        // b * H_kv + kh
-  const int n_mt = gridDim.y;
-  const int mt = n_mt - 1 - (int)blockIdx.y;          // longest tiles first
+  const int unit = blockIdx.x;
+  const int mt = (int)gridDim.y - 1 - (int)blockIdx.y;   // longest tiles first
   const int b = unit / p.H_kv, kh = unit % p.H_kv;
   const int m0 = mt * BM;
   const int S = p.S;
-  const int kv_end = min(m0 + BM, S);
-  const int ntiles = (kv_end + BN - 1) / BN;
+  const int ntiles = (min(m0 + BM, S) + BN - 1) / BN;
   const int H_q = p.H_kv * G;
 
-  auto stage_k = [&](int s, int src) { return sKV + (size_t)(s * 2 * NSRC + src) * Cfg::KV_BYTES; };
+  auto stage_k = [&](int s, int src) { return sKV + (size_t)s * PL::STAGE + (size_t)src * Cfg::KV_BYTES; };
   auto stage_v = [&](int s, int src) {
-    return sKV + (size_t)(s * 2 * NSRC + NSRC + src) * Cfg::KV_BYTES;
+    return sKV + (size_t)s * PL::STAGE + (size_t)(NSRC + src) * Cfg::KV_BYTES;
+  };
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(bar, parity)) return true;
+    *abort_flag = 1;
+    flag_status(p.status, kDevTimeout);
+    return false;
   };
 
   if (tid == 0) {
-    mbar_init(&bar_full[0], 1);
-    mbar_init(&bar_full[1], 1);
     mbar_init(bar_q, 1);
-    mbar_init(bar_mma, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_ready[s], 128);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int h = 0; h < G; ++h) {
+      mbar_init(&s_full[2 * h], 1);
+      mbar_init(&s_full[2 * h + 1], 1);
+      mbar_init(&p_full[h], 128);
+      mbar_init(&o_done[h], 1);
+    }
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (NSRC == 2) {
-    for (int i = tid; i < D; i += NT) {
+    for (int i = tid; i < D; i += PL::THREADS) {
       sW[i] = p.a0[kh * D + i];
       sW[D + i] = p.a1[kh * D + i];
       sW[2 * D + i] = p.b0[kh * D + i];
       sW[3 * D + i] = p.b1[kh * D + i];
     }
   }
-  if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == PL::MMA_WARP) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  auto load_tile = [&](int j) {
-    const int s = j & 1;
-    const int n0 = j * BN;
-    mbar_arrive_expect_tx(&bar_full[s], 2 * NSRC * Cfg::KV_BYTES);
-    for (int cb = 0; cb < CB; ++cb) {
-      tma_load_3d(stage_k(s, 0) + cb * BN * SW, &maps.k0, cb * SWE, n0, unit, &bar_full[s]);
-      tma_load_3d(stage_v(s, 0) + cb * BN * SW, &maps.v0, cb * SWE, n0, unit, &bar_full[s]);
-      if (NSRC == 2) {
-        tma_load_3d(stage_k(s, 1) + cb * BN * SW, &maps.k1, cb * SWE, n0, unit, &bar_full[s]);
-        tma_load_3d(stage_v(s, 1) + cb * BN * SW, &maps.v1, cb * SWE, n0, unit, &bar_full[s]);
-      }
-    }
-  };
-
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_q, G * Cfg::Q_BYTES);
-    for (int h = 0; h < G; ++h)
-      for (int cb = 0; cb < CB; ++cb)
-        tma_load_3d(sQ + h * Cfg::Q_BYTES + cb * BM * SW, &maps.q, cb * SWE, m0,
-                    b * H_q + kh * G + h, bar_q);
-    load_tile(0);
-    if (ntiles > 1) load_tile(1);
-  }
-
-  // softmax state: thread owns query row `row` of head `hh`
-  const int hh = warp >> 2;
-  const int quarter = warp & 3;
-  const int row = quarter * 32 + lane;
-  const int qpos = m0 + row;
-  const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-  const uint32_t t_s = tmem + lane_addr + hh * HEAD_COLS;
-  const uint32_t t_o = t_s + BN;
-  float m_run = -FLT_MAX, l_run = 0.f;
-  uint32_t mma_phase = 0;
-  bool failed = false;
-
-  constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
-  constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, true);
-
-  {
-    bool bad = !mbar_wait_bounded(bar_q, 0);
-    if (__syncthreads_or(bad)) failed = true;
-  }
-
-  for (int j = 0; j < ntiles && !failed; ++j) {
-    const int s = j & 1;
-    const int n0 = j * BN;
-    {
-      bool bad = !mbar_wait_bounded(&bar_full[s], (uint32_t)(j >> 1) & 1u);
-      if (__syncthreads_or(bad)) { failed = true; break; }
-    }
-    if (NSRC == 2) {
-      // K = a0 (.) K0 + a1 (.) K1 and V = b0 (.) V0 + b1 (.) V1, fp32 -> bf16,
-      // written over source 0 in the same swizzled layout.
-      constexpr int CHUNKS = CB * BN * (SW / 16);
-#pragma unroll 1
-      for (int t = 0; t < 2; ++t) {
-        uint8_t* d0 = t == 0 ? stage_k(s, 0) : stage_v(s, 0);
-        const uint8_t* d1 = t == 0 ? stage_k(s, 1) : stage_v(s, 1);
-        const float* w0 = sW + (t == 0 ? 0 : 2 * D);
-        const float* w1 = sW + (t == 0 ? D : 3 * D);
-        for (int c = tid; c < CHUNKS; c += NT) {
-          const int cb = c / (BN * 4);
-          const int r = (c / 4) % BN;
-          const int pc = c & 3;
-          const int lc = pc ^ ((r >> 1) & 3);
-          const int col = cb * SWE + lc * 8;
-          uint4* p0 = reinterpret_cast<uint4*>(d0 + (size_t)c * 16);
-          const uint4 x = *p0;
-          const uint4 y = *reinterpret_cast<const uint4*>(d1 + (size_t)c * 16);
-          if (col >= D) continue;  // padding columns stay zero
-          float fx[8], fy[8];
-          unpack16<__nv_bfloat16>(x, fx);
-          unpack16<__nv_bfloat16>(y, fy);
-          uint32_t o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = w0[col + 2 * e] * fx[2 * e] + w1[col + 2 * e] * fy[2 * e];
-            const float hi = w0[col + 2 * e + 1] * fx[2 * e + 1] + w1[col + 2 * e + 1] * fy[2 * e + 1];
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(lo, hi);
-            o[e] = *reinterpret_cast<uint32_t*>(&v2);
+  if (warp == PL::PRODUCER_WARP) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_q, G * Cfg::Q_BYTES);
+      for (int h = 0; h < G; ++h)
+        for (int cb = 0; cb < CB; ++cb)
+          tma_load_3d(sQ + h * Cfg::Q_BYTES + cb * BM * SW, &maps.q, cb * SWE, m0,
+                      b * H_q + kh * G + h, bar_q);
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % NS, u = j / NS;
+        if (u > 0 && !wait(&kv_empty[s], (uint32_t)(u - 1) & 1u)) break;
+        const int n0 = j * BN;
+        mbar_arrive_expect_tx(&kv_full[s], PL::STAGE);
+        for (int cb = 0; cb < CB; ++cb) {
+          tma_load_3d(stage_k(s, 0) + cb * BN * SW, &maps.k0, cb * SWE, n0, unit, &kv_full[s]);
+          tma_load_3d(stage_v(s, 0) + cb * BN * SW, &maps.v0, cb * SWE, n0, unit, &kv_full[s]);
+          if (NSRC == 2) {
+            tma_load_3d(stage_k(s, 1) + cb * BN * SW, &maps.k1, cb * SWE, n0, unit, &kv_full[s]);
+            tma_load_3d(stage_v(s, 1) + cb * BN * SW, &maps.v1, cb * SWE, n0, unit, &kv_full[s]);
           }
-          *p0 = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
-      fence_proxy_async_smem();
-      __syncthreads();
     }
-
-    // S_h = Q_h K^T for every head
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t kbase = smem_u32(stage_k(s, 0));
+  } else if (warp == PL::MMA_WARP) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, true);
+      uint64_t* ready = NSRC == 2 ? kv_ready : kv_full;
+      auto issue_qk = [&](int j) {
+        const int s = j % NS;
+        const uint32_t kbase = smem_u32(stage_k(s, 0));
+        for (int h = 0; h < G; ++h) {
+          const uint32_t qbase = smem_u32(sQ + h * Cfg::Q_BYTES);
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const uint32_t qbase = smem_u32(sQ + h * Cfg::Q_BYTES);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (uint32_t)(k & 1) * 32;
-          const uint64_t ad = sdesc(qbase + (k >> 1) * BM * SW + off, 16, 8 * SW);
-          const uint64_t bd = sdesc(kbase + (k >> 1) * BN * SW + off, 16, 8 * SW);
-          mma_bf16(tmem + h * HEAD_COLS, ad, bd, IDESC_QK, k > 0);
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (uint32_t)(k & 1) * 32;
+            const uint64_t ad = sdesc(qbase + (k >> 1) * BM * SW + off, 16, 8 * SW);
+            const uint64_t bd = sdesc(kbase + (k >> 1) * BN * SW + off, 16, 8 * SW);
+            mma_bf16(tmem + h * HEAD_COLS + (j & 1) * BN, ad, bd, IDESC_QK, k > 0);
+          }
+          mma_commit(&s_full[2 * h + (j & 1)]);
         }
+      };
+      bool ok = wait(bar_q, 0) && wait(&ready[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0);
       }
-      mma_commit(bar_mma);
-    }
-    {
-      bool bad = !mbar_wait_bounded(bar_mma, mma_phase);
-      mma_phase ^= 1u;
-      if (__syncthreads_or(bad)) { failed = true; break; }
-    }
-    tc_fence_after();
-
-    // Online softmax of this thread's row.
-    float sv[BN];
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (j + 1 < ntiles) {
+          const int s1 = (j + 1) % NS;
+          if (!wait(&ready[s1], (uint32_t)((j + 1) / NS) & 1u)) break;
+          tc_fence_after();
+          issue_qk(j + 1);
+        }
+        const int s = j % NS;
+        const uint32_t vbase = smem_u32(stage_v(s, 0));
+        for (int h = 0; h < G; ++h) {
+          if (!wait(&p_full[h], (uint32_t)j & 1u)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t pbase = smem_u32(sP + h * Cfg::P_BYTES);
 #pragma unroll
-    for (int c = 0; c < BN; c += 16) tmem_ld16(t_s + c, sv + c);
-    tmem_wait_ld();
-    float mt_row = -FLT_MAX;
-#pragma unroll
-    for (int c = 0; c < BN; ++c) {
-      const int kp = n0 + c;
-      const bool ok = kp <= qpos && kp < S;
-      sv[c] = ok ? sv[c] * p.scale_log2 : -FLT_MAX;
-      mt_row = fmaxf(mt_row, sv[c]);
+          for (int k = 0; k < BN / 16; ++k) {
+            const uint64_t ad = sdesc(pbase + (k >> 1) * BM * SW + (k & 1) * 32, 16, 8 * SW);
+            const uint64_t bd = sdesc(vbase + k * 16 * SW, BN * SW, 8 * SW);
+            mma_bf16(tmem + h * HEAD_COLS + 2 * BN, ad, bd, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&o_done[h]);
+        }
+        if (!ok) break;
+        mma_commit(&kv_empty[s]);
+      }
     }
-    const float m_new = fmaxf(m_run, mt_row);
-    const float alpha = fast_exp2(m_run - m_new);
-    float psum = 0.f;
+  } else if (warp >= PL::SOFTMAX_WARPS) {
+    // ---------------- fusion warpgroup (fused mode) ----------------
+    if constexpr (NSRC == 2) {
+      const int ft = tid - 32 * PL::SOFTMAX_WARPS;   // 0..127
+      constexpr int CHUNKS = CB * BN * (SW / 16);
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % NS;
+        if (!wait(&kv_full[s], (uint32_t)(j / NS) & 1u)) break;
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          uint8_t* d0 = t == 0 ? stage_k(s, 0) : stage_v(s, 0);
+          const uint8_t* d1 = t == 0 ? stage_k(s, 1) : stage_v(s, 1);
+          const float* w0 = sW + (t == 0 ? 0 : 2 * D);
+          const float* w1 = sW + (t == 0 ? D : 3 * D);
+          for (int c = ft; c < CHUNKS; c += 128) {
+            const int cb = c / (BN * 4);
+            const int r = (c / 4) % BN;
+            const int lc = (c & 3) ^ ((r >> 1) & 3);
+            const int col = cb * SWE + lc * 8;
+            if (col >= D) continue;  // padding columns stay zero
+            uint4* p0 = reinterpret_cast<uint4*>(d0 + (size_t)c * 16);
+            const uint4 x = *p0;
+            const uint4 y = *reinterpret_cast<const uint4*>(d1 + (size_t)c * 16);
+            const float4 wa = *reinterpret_cast<const float4*>(w0 + col);
+            const float4 wb = *reinterpret_cast<const float4*>(w0 + col + 4);
+            const float4 va = *reinterpret_cast<const float4*>(w1 + col);
+            const float4 vb = *reinterpret_cast<const float4*>(w1 + col + 4);
+            const float u0[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+            const float u1[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+            float fx[8], fy[8];
+            unpack16<__nv_bfloat16>(x, fx);
+            unpack16<__nv_bfloat16>(y, fy);
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = fmaf(u0[2 * e], fx[2 * e], u1[2 * e] * fy[2 * e]);
+              const float hi = fmaf(u0[2 * e + 1], fx[2 * e + 1], u1[2 * e + 1] * fy[2 * e + 1]);
+              __nv_bfloat162 v2 = __floats2bfloat162_rn(lo, hi);
+              o[e] = *reinterpret_cast<uint32_t*>(&v2);
+            }
+            *p0 = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&kv_ready[s]);
+      }
+    }
+  } else {
+    // ---------------- softmax warpgroup of head hh ----------------
+    const int hh = warp >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int qpos = m0 + row;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_head = tmem + lane_addr + hh * HEAD_COLS;
+    const uint32_t t_o = t_head + 2 * BN;
     uint8_t* prow = sP + hh * Cfg::P_BYTES;
+    float m_run = -FLT_MAX, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int n0 = j * BN;
+      // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
+      if (!__all_sync(0xffffffffu, wait(&s_full[2 * hh + (j & 1)], (uint32_t)(j >> 1) & 1u))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[BN];
 #pragma unroll
-    for (int c = 0; c < BN; c += 8) {
-      uint32_t pk[4];
+      for (int c = 0; c < BN; c += 16) tmem_ld16(t_head + (j & 1) * BN + c, sv + c);
+      tmem_wait_ld();
+      const bool diag = n0 + BN > m0 || n0 + BN > S;   // warp-uniform
+      float mt_row = -FLT_MAX;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x0 = sv[c + 2 * e] == -FLT_MAX ? 0.f : fast_exp2(sv[c + 2 * e] - m_new);
-        const float x1 = sv[c + 2 * e + 1] == -FLT_MAX ? 0.f : fast_exp2(sv[c + 2 * e + 1] - m_new);
+      for (int c = 0; c < BN; ++c) {
+        float x = sv[c] * p.scale_log2;
+        if (diag) {
+          const int kp = n0 + c;
+          if (kp > qpos || kp >= S) x = -FLT_MAX;
+        }
+        sv[c] = x;
+        mt_row = fmaxf(mt_row, x);
+      }
+      // Keep a stale max until it is exceeded by more than 2^8: P stays
+      // below 256 (exact in bf16 and fp32) and O needs no rescaling.
+      const float m_new = mt_row > m_run + RESCALE_SLACK ? mt_row : m_run;
+      const float alpha = fast_exp2(m_run - m_new);
+      float psum = 0.f;
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) {
+        const float x0 = sv[c] == -FLT_MAX ? 0.f : fast_exp2(sv[c] - m_new);
+        const float x1 = sv[c + 1] == -FLT_MAX ? 0.f : fast_exp2(sv[c + 1] - m_new);
         psum += x0 + x1;
         __nv_bfloat162 v2 = __floats2bfloat162_rn(x0, x1);
-        pk[e] = *reinterpret_cast<uint32_t*>(&v2);
+        pk[c / 2] = *reinterpret_cast<uint32_t*>(&v2);
       }
-      const int blk = c / SWE, lc = (c % SWE) / 8;
-      *reinterpret_cast<uint4*>(prow + blk * BM * SW + swz64(row, lc)) =
-          make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+      if (j > 0) {
+        // PV of tile j-1 must be done: it reads P_h and accumulates O_h
+        if (!__all_sync(0xffffffffu, wait(&o_done[hh], (uint32_t)(j - 1) & 1u))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D; c += 16) {
+            float ov[16];
+            tmem_ld16(t_o + c, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] *= alpha;
+            tmem_st16(t_o + c, ov);
+          }
+          tmem_wait_st();
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < BN; c += 8) {
+        const int blk = c / SWE, lc = (c % SWE) / 8;
+        *reinterpret_cast<uint4*>(prow + blk * BM * SW + swz64(row, lc)) =
+            make_uint4(pk[c / 2], pk[c / 2 + 1], pk[c / 2 + 2], pk[c / 2 + 3]);
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(&p_full[hh]);
     }
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-    if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+    if (ok && __all_sync(0xffffffffu, wait(&o_done[hh], (uint32_t)(ntiles - 1) & 1u))) {
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                            (((size_t)b * H_q + kh * G + hh) * S + qpos) * D;
 #pragma unroll
       for (int c = 0; c < D; c += 16) {
         float ov[16];
         tmem_ld16(t_o + c, ov);
         tmem_wait_ld();
+        uint32_t q8[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ov[e] *= alpha;
-        tmem_st16(t_o + c, ov);
-      }
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    // O_h += P_h V
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t vbase = smem_u32(stage_v(s, 0));
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const uint32_t pbase = smem_u32(sP + h * Cfg::P_BYTES);
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t ad = sdesc(pbase + (k >> 1) * BM * SW + (k & 1) * 32, 16, 8 * SW);
-          const uint64_t bd = sdesc(vbase + k * 16 * SW, BN * SW, 8 * SW);
-          mma_bf16(tmem + h * HEAD_COLS + BN, ad, bd, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
+        for (int e = 0; e < 8; ++e) {
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(ov[2 * e] * inv, ov[2 * e + 1] * inv);
+          q8[e] = *reinterpret_cast<uint32_t*>(&v2);
+        }
+        if (qpos < S) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+          dst[0] = make_uint4(q8[0], q8[1], q8[2], q8[3]);
+          dst[1] = make_uint4(q8[4], q8[5], q8[6], q8[7]);
         }
       }
-      mma_commit(bar_mma);
-    }
-    {
-      bool bad = !mbar_wait_bounded(bar_mma, mma_phase);
-      mma_phase ^= 1u;
-      if (__syncthreads_or(bad)) { failed = true; break; }
-    }
-    tc_fence_after();
-    // stage s is free again: prefetch tile j + 2 into it
-    if (tid == 0 && j + 2 < ntiles) {
-      fence_proxy_async_smem();
-      load_tile(j + 2);
     }
   }
 
-  if (failed) {
-    if (tid == 0) flag_status(p.status, kDevTimeout);
-  } else {
-    // Epilogue: O_h / l -> bf16 rows of out[b, kh*G + hh, m0 + row, :].
-    const float inv = 1.f / l_run;
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                          (((size_t)b * H_q + kh * G + hh) * S + qpos) * D;
-#pragma unroll
-    for (int c = 0; c < D; c += 16) {
-      float ov[16];
-      tmem_ld16(t_o + c, ov);
-      tmem_wait_ld();
-      uint32_t pk[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        __nv_bfloat162 v2 = __floats2bfloat162_rn(ov[2 * e] * inv, ov[2 * e + 1] * inv);
-        pk[e] = *reinterpret_cast<uint32_t*>(&v2);
-      }
-      if (qpos < S) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
-        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      }
-    }
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+  if (*abort_flag) {
+    // let the copies still in flight land before the CTA exits
+    for (int s = 0; s < NS && tid == 0; ++s) (void)mbar_wait_bounded(&kv_full[s], 0, kDrainLimitNs);
+  }
+  if (warp == PL::MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
 }
 
 // --- host side ---------------------------------------------------------------
@@ -533,7 +602,7 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)units, (unsigned)((a.S + BM - 1) / BM));
-  kern<<<grid, 128 * G, smem, stream>>>(maps, p);
+  kern<<<grid, PrefillPlan<D, NSRC, G>::THREADS, smem, stream>>>(maps, p);
   return cudaGetLastError();
 }
 
