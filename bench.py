@@ -341,6 +341,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=4.0)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-other-decode", action="store_true",
+                    help="skip the single-call timings of the 1.5B and 4B decode workloads")
     ap.add_argument("--profile", default=None,
                     help="run one call type only, e.g. decode:fused:332M-decode or "
                          "prefill:fused:650M-prefill (for ncu captures)")
@@ -425,13 +427,16 @@ def main():
            "note": "fused step via the C ABI; per-step q and new K/V from pinned host memory, "
                    "all 12 layer outputs read back, host sync every step"}
 
-    prefill = None
-    if not args.no_prefill:
-        prefill = bench_prefill(device, stream, peaks, W)
-
     model.close()
     del model
     torch.cuda.empty_cache()
+
+    prefill = None
+    if not args.no_prefill:
+        prefill = bench_prefill(device, stream, peaks, W)
+    other_decode = None
+    if not args.no_other_decode:
+        other_decode = bench_decode_calls(device, stream, peaks, W)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -468,63 +473,105 @@ def main():
         }
         if prefill is not None:
             line["prefill"] = prefill
+        if other_decode is not None:
+            line["decode_other_workloads"] = other_decode
         print(json.dumps(line), flush=True)
     if dist_on:
         torch.distributed.destroy_process_group()
 
 
+class SingleCall:
+    """Buffers for one call type of a workload: only the layers it reads."""
+
+    def __init__(self, kind, mode, w, device, stream):
+        import cross_layer_kv_gb300 as fkv
+        from cross_layer_kv_gb300 import synth
+        self.w, self.kind, self.mode = w, kind, mode
+        layer = w.num_layers
+        need = [layer] if mode == "vanilla" else sorted({1, w.n})
+        self.ctx = fkv.Context(w.num_layers, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim,
+                               w.dtype, store_upper=(mode == "vanilla"))
+        self.keep = []
+        for l in need:
+            k, v = synth.make_cache(w, l, 0, device)
+            self.keep.append((k, v))
+            self.ctx.fkv_bind_layer_cache(l, k, v)
+        wts = synth.make_weights(w, layer, 0, device)
+        self.keep.append(wts)
+        self.ctx.fkv_set_fusion_weights(layer, *wts)
+        ctx = self.ctx
+        if kind == "decode":
+            q = synth.make_query(w, layer, 0, device)
+            out = torch.empty_like(q)
+            lens = synth.make_seq_lens(w, 0, device)
+            ws = ctx.workspace(device)
+            self.keep += [q, out, lens, ws]
+            self.call = lambda: ctx.fkv_decode_attn(q, layer, mode, lens, out, ws, stream)
+            nsrc = 2 if mode == "fused" else 1
+            self.bytes = 2 * nsrc * w.kv_heads * int(lens.sum()) * w.head_dim * w.elem_bytes
+            self.flops = 0
+        else:
+            q = synth.make_query(w, layer, 0, device, positions=w.seq)
+            out = torch.empty_like(q)
+            self.keep += [q, out]
+            self.call = lambda: ctx.fkv_prefill_attn(q, layer, mode, w.seq, out, stream)
+            self.bytes = 0
+            self.flops = 4.0 * w.batch * w.q_heads * w.head_dim * w.seq * (w.seq + 1) / 2
+
+    def time_us(self, stream, steps, warmup):
+        for _ in range(warmup):
+            self.call()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            self.call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / steps
+
+    def close(self):
+        self.ctx.close()
+        self.keep.clear()
+
+
 def run_profile_case(args, device):
     """One call type on its own, W warm-up calls then K timed calls; prints
     the mean call time.  Used for ncu captures of a single kernel."""
-    import cross_layer_kv_gb300 as fkv
     from cross_layer_kv_gb300 import synth
     kind, mode, wname = args.profile.split(":")
-    w = synth.WORKLOADS[wname]
-    layer = w.num_layers
-    n = w.n
-    need = [layer] if mode == "vanilla" else sorted({1, n})
-    ctx = fkv.Context(w.num_layers, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim, w.dtype,
-                      store_upper=(mode == "vanilla"))
-    keep = []
-    for l in need:
-        k, v = synth.make_cache(w, l, 0, device)
-        keep.append((k, v))
-        ctx.fkv_bind_layer_cache(l, k, v)
-    wts = synth.make_weights(w, layer, 0, device)
-    ctx.fkv_set_fusion_weights(layer, *wts)
     stream = torch.cuda.Stream(device)
-    if kind == "decode":
-        q = synth.make_query(w, layer, 0, device)
-        out = torch.empty_like(q)
-        lens = synth.make_seq_lens(w, 0, device)
-        ws = ctx.workspace(device)
-        call = lambda: ctx.fkv_decode_attn(q, layer, mode, lens, out, ws, stream)
-        nbytes = (4 if mode == "fused" else 2) * w.kv_heads * int(lens.sum()) * w.head_dim * w.elem_bytes
-    else:
-        q = synth.make_query(w, layer, 0, device, positions=w.seq)
-        out = torch.empty_like(q)
-        call = lambda: ctx.fkv_prefill_attn(q, layer, mode, w.seq, out, stream)
-        nbytes = 0
-    for _ in range(args.warmup):
-        call()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    sc = SingleCall(kind, mode, synth.WORKLOADS[wname], device, stream)
+    us = sc.time_us(stream, args.steps, args.warmup)
     res = {"profile": args.profile, "call_us": us}
-    if nbytes:
-        res["GBps"] = nbytes / (us * 1e-6) / 1e9
-        res["bytes"] = nbytes
+    if sc.bytes:
+        res["GBps"] = sc.bytes / (us * 1e-6) / 1e9
+        res["bytes"] = sc.bytes
     else:
-        flops = 4.0 * w.batch * w.q_heads * w.head_dim * w.seq * (w.seq + 1) / 2
-        res["TFLOPs"] = flops / (us * 1e-6) / 1e12
+        res["TFLOPs"] = sc.flops / (us * 1e-6) / 1e12
     print(json.dumps(res), flush=True)
-    ctx.close()
+    sc.close()
+
+
+def bench_decode_calls(device, stream, peaks, W, reps=20):
+    """One upper-layer decode call per mode of the other decode workloads
+    (1.5B-shaped ragged, 4B-shaped 128k): time, GB/s, % of 8 TB/s."""
+    from cross_layer_kv_gb300 import synth
+    res = {}
+    for w in (synth.B1_5, synth.B4):
+        res[w.name] = {}
+        for mode in ("vanilla", "lite", "fused"):
+            sc = SingleCall("decode", mode, w, device, stream)
+            us = sc.time_us(stream, reps, W)
+            gbs = sc.bytes / (us * 1e-6) / 1e9
+            res[w.name][mode] = {"upper_call_us": us, "bytes": sc.bytes, "GBps": gbs,
+                                 "pct_of_8TBps": 100.0 * gbs / HBM_REF_GBS,
+                                 "pct_of_measured_hbm": 100.0 * gbs / peaks["hbm_gbs"]}
+            sc.close()
+            del sc
+            torch.cuda.empty_cache()
+    return res
 
 
 def bench_prefill(device, stream, peaks, W):

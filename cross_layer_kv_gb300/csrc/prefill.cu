@@ -131,6 +131,29 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// (c0, c1) += (a0, a1) * (b0, b1): one packed fp32 FMA.
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 A, B, C;\n\t"
+      "mov.b64 A, {%2, %3};\n\t"
+      "mov.b64 B, {%4, %5};\n\t"
+      "mov.b64 C, {%0, %1};\n\t"
+      "fma.rn.f32x2 C, A, B, C;\n\t"
+      "mov.b64 {%0, %1}, C;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// (c0, c1) += (a0, a1): one packed fp32 add.
+__device__ __forceinline__ void add2(float& c0, float& c1, float a0, float a1) {
+  asm("{\n\t.reg .b64 A, C;\n\t"
+      "mov.b64 A, {%2, %3};\n\t"
+      "mov.b64 C, {%0, %1};\n\t"
+      "add.rn.f32x2 C, C, A;\n\t"
+      "mov.b64 {%0, %1}, C;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1));
+}
+
 // Shared-memory matrix descriptor of tcgen05 (start, leading and stride byte
 // offsets, descriptor version 1, swizzle mode 4 = 64-byte swizzle).
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -440,31 +463,41 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       for (int c = 0; c < BN; c += 16) tmem_ld16(t_head + (j & 1) * BN + c, sv + c);
       tmem_wait_ld();
       const bool diag = n0 + BN > m0 || n0 + BN > S;   // warp-uniform
-      float mt_row = -FLT_MAX;
+      if (diag) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        float x = sv[c] * p.scale_log2;
-        if (diag) {
+        for (int c = 0; c < BN; ++c) {
           const int kp = n0 + c;
-          if (kp > qpos || kp >= S) x = -FLT_MAX;
+          if (kp > qpos || kp >= S) sv[c] = -INFINITY;
         }
-        sv[c] = x;
-        mt_row = fmaxf(mt_row, x);
       }
+      // row max of the raw scores (the scale is positive, so it commutes)
+      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+      for (int c = 4; c < BN; c += 4) {
+        mx0 = fmaxf(mx0, sv[c]);
+        mx1 = fmaxf(mx1, sv[c + 1]);
+        mx2 = fmaxf(mx2, sv[c + 2]);
+        mx3 = fmaxf(mx3, sv[c + 3]);
+      }
+      const float mt_row = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
       // Keep a stale max until it is exceeded by more than 2^8: P stays
       // below 256 (exact in bf16 and fp32) and O needs no rescaling.
       const float m_new = mt_row > m_run + RESCALE_SLACK ? mt_row : m_run;
       const float alpha = fast_exp2(m_run - m_new);
-      float psum = 0.f;
+      const float neg_m = -m_new;
+      float ps0 = 0.f, ps1 = 0.f;
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN; c += 2) {
-        const float x0 = sv[c] == -FLT_MAX ? 0.f : fast_exp2(sv[c] - m_new);
-        const float x1 = sv[c + 1] == -FLT_MAX ? 0.f : fast_exp2(sv[c + 1] - m_new);
-        psum += x0 + x1;
-        __nv_bfloat162 v2 = __floats2bfloat162_rn(x0, x1);
+        // x = s * scale - m for two scores with one packed FMA; exp2(-inf) = 0
+        float x0 = neg_m, x1 = neg_m;
+        fma2(x0, x1, sv[c], sv[c + 1], p.scale_log2, p.scale_log2);
+        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+        add2(ps0, ps1, e0, e1);
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(e0, e1);
         pk[c / 2] = *reinterpret_cast<uint32_t*>(&v2);
       }
+      const float psum = ps0 + ps1;
       l_run = l_run * alpha + psum;
       m_run = m_new;
       if (j > 0) {
