@@ -227,6 +227,43 @@ def prefill_attn(q, layer, num_layers, mode, k_caches, v_caches,
     return prefill_attention(q, k_i, v_i, scale, rows)
 
 
+def chunk_prefill_attention(q: np.ndarray, q_start: int, k: np.ndarray, v: np.ndarray,
+                            scale: Optional[float] = None) -> np.ndarray:
+    """Causal attention of a chunk of queries over an existing cache.
+
+    q ``[B, H_q, C, D]`` holds the queries of positions q_start .. q_start+C-1;
+    k, v ``[B, H_kv, >= q_start+C, D]``.  Query i sees key positions
+    t <= q_start + i (the prompt rows before the chunk are already cached).
+    With q_start = 0 this is ``prefill_attention``; with C = 1 it is one
+    decode step over q_start + 1 cached rows.
+    """
+    B, H_q, C, D = q.shape
+    H_kv = k.shape[1]
+    G = H_q // H_kv
+    if scale is None:
+        scale = default_scale(D)
+    out = np.empty((B, H_q, C, D), dtype=np.float64)
+    for b in range(B):
+        for h in range(H_q):
+            kv = h // G
+            for i in range(C):
+                n = q_start + i + 1
+                out[b, h, i] = attend(q[b, h, i], k[b, kv, :n], v[b, kv, :n], scale)
+    return out
+
+
+def chunk_prefill_attn(q, q_start, layer, num_layers, mode, k_caches, v_caches, weights=None,
+                       scale=None, k_sources=None, v_sources=None):
+    """A chunked causal prefill call of one layer: reconstruct rows
+    [0, q_start + C), then attend."""
+    n = q_start + q.shape[2]
+    k_i, v_i = reconstruct_kv(layer, num_layers, mode,
+                              {l: c[:, :, :n] for l, c in k_caches.items()},
+                              {l: c[:, :, :n] for l, c in v_caches.items()},
+                              weights, k_sources, v_sources)
+    return chunk_prefill_attention(q, q_start, k_i, v_i, scale)
+
+
 # ---------------------------------------------------------------------------
 # Cache append ([Notes] §2.3: the storage caches take the new token's
 # post-RoPE K/V before the upper layers attend)

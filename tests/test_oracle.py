@@ -431,3 +431,39 @@ def test_append_writes_rows_at_offsets_only():
     np.testing.assert_array_equal(out[1, :, :7], cache[1, :, :7])
     with pytest.raises(ValueError):
         O.append_kv(cache, new, [8, 0])
+
+
+# --------------------------------------------------------------------------
+# chunked prefill over an existing cache (a prompt continued in chunks)
+# --------------------------------------------------------------------------
+
+def test_chunk_prefill_matches_sdpa_with_offset_mask():
+    """Library pin: SDPA with an explicit boolean mask allowing key t for
+    query i iff t <= q_start + i."""
+    rng = _rng(20)
+    B, H_kv, G, D, q_start, C = 2, 2, 2, 8, 11, 7
+    n = q_start + C
+    q = rng.standard_normal((B, H_kv * G, C, D))
+    k = rng.standard_normal((B, H_kv, n + 3, D))
+    v = rng.standard_normal((B, H_kv, n + 3, D))
+    got = O.chunk_prefill_attention(q, q_start, k, v)
+    mask = torch.tensor([[t <= q_start + i for t in range(n)] for i in range(C)])
+    qt = torch.from_numpy(q)
+    kt = torch.from_numpy(k[:, :, :n]).repeat_interleave(G, dim=1)
+    vt = torch.from_numpy(v[:, :, :n]).repeat_interleave(G, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask).numpy()
+    np.testing.assert_allclose(got, ref, atol=1e-12)
+
+
+def test_chunks_reassemble_full_prefill_and_last_row_is_decode():
+    rng = _rng(21)
+    L, B, H_kv, S, D = 4, 1, 2, 30, 8
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2])
+    ws = {3: _weights(rng, H_kv, D)}
+    q = rng.standard_normal((B, 4, S, D))
+    full = O.prefill_attn(q, 3, L, O.FUSED, kc, vc, weights=ws)
+    parts = [O.chunk_prefill_attn(q[:, :, a:b], a, 3, L, O.FUSED, kc, vc, weights=ws)
+             for a, b in ((0, 9), (9, 10), (10, 30))]
+    np.testing.assert_allclose(np.concatenate(parts, axis=2), full, atol=1e-12)
+    last = O.decode_attn(q[:, :, S - 1], 3, L, O.FUSED, kc, vc, [S], weights=ws)
+    np.testing.assert_allclose(full[:, :, S - 1], last, atol=1e-12)
