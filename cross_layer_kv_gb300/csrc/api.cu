@@ -230,13 +230,20 @@ fkv_status fkv_decode_attn(fkv_ctx* c, const void* q, int layer, int mode,
 
 fkv_status fkv_prefill_attn(fkv_ctx* c, const void* q, int layer, int mode, int S, void* out,
                             void* stream) {
+  return fkv_prefill_attn_chunk(c, q, layer, mode, 0, S, out, stream);
+}
+
+fkv_status fkv_prefill_attn_chunk(fkv_ctx* c, const void* q, int layer, int mode, int q_start,
+                                  int C, void* out, void* stream) {
   if (!c) return FKV_ERR_INVALID_ARG;
+  const int S = C;
   fkv::PrefillArgs p{};
   fkv_status s = resolve_sources(c, layer, mode, p.k, p.v, p.a, p.b, &p.nsrc);
   if (s != FKV_OK) return s;
   if (c->cfg.dtype != FKV_BF16) return FKV_ERR_UNSUPPORTED;
-  if (S < 1 || S > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
+  if (S < 1 || q_start < 0 || (long long)q_start + S > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return FKV_ERR_INVALID_ARG;
+  p.q_start = q_start;
   p.q = q;
   p.out = out;
   p.status = c->status;

@@ -87,6 +87,7 @@ struct PrefillArgs {
   void* out;       // [B, H_q, S, D] bf16
   int* status;
   int batch, kv_heads, group, max_seq, head_dim, S;
+  int q_start;     // cache position of query row 0 (0 for a whole prompt)
   int nsrc;
   float softmax_scale;
 };

@@ -193,7 +193,10 @@ struct PrefillParams {
   const float* b1;
   void* out;
   int* status;
-  int B, H_kv, S;
+  int B, H_kv;
+  int S;        // query rows of this call (the chunk length C)
+  int q_start;  // cache position of the first query row
+  int S_kv;     // key rows attended: q_start + C
   float scale_log2;
 };
 
@@ -270,9 +273,11 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   const int unit = blockIdx.x;
   const int mt = (int)gridDim.y - 1 - (int)blockIdx.y;   // longest tiles first
   const int b = unit / p.H_kv, kh = unit % p.H_kv;
-  const int m0 = mt * BM;
-  const int S = p.S;
-  const int ntiles = (min(m0 + BM, S) + BN - 1) / BN;
+  const int m0 = mt * BM;              // first query row of the tile (within the chunk)
+  const int S = p.S;                   // query rows
+  const int S_kv = p.S_kv;             // key rows
+  const int pos0 = p.q_start + m0;     // cache position of query row m0
+  const int ntiles = (min(pos0 + BM, S_kv) + BN - 1) / BN;
   const int H_q = p.H_kv * G;
 
   auto stage_k = [&](int s, int src) { return sKV + (size_t)s * PL::STAGE + (size_t)src * Cfg::KV_BYTES; };
@@ -443,7 +448,8 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     const int hh = warp >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int qpos = m0 + row;
+    const int qpos = pos0 + row;         // cache position of this query
+    const bool row_valid = m0 + row < S;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const uint32_t t_head = tmem + lane_addr + hh * HEAD_COLS;
     const uint32_t t_o = t_head + 2 * BN;
@@ -462,12 +468,12 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < BN; c += 16) tmem_ld16(t_head + (j & 1) * BN + c, sv + c);
       tmem_wait_ld();
-      const bool diag = n0 + BN > m0 || n0 + BN > S;   // warp-uniform
+      const bool diag = n0 + BN > pos0 || n0 + BN > S_kv;   // warp-uniform
       if (diag) {
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const int kp = n0 + c;
-          if (kp > qpos || kp >= S) sv[c] = -INFINITY;
+          if (kp > qpos || kp >= S_kv) sv[c] = -INFINITY;
         }
       }
       // row max of the raw scores (the scale is positive, so it commutes)
@@ -534,7 +540,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       tc_fence_after();
       const float inv = 1.f / l_run;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                            (((size_t)b * H_q + kh * G + hh) * S + qpos) * D;
+                            (((size_t)b * H_q + kh * G + hh) * S + m0 + row) * D;
 #pragma unroll
       for (int c = 0; c < D; c += 16) {
         float ov[16];
@@ -546,7 +552,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
           __nv_bfloat162 v2 = __floats2bfloat162_rn(ov[2 * e] * inv, ov[2 * e + 1] * inv);
           q8[e] = *reinterpret_cast<uint32_t*>(&v2);
         }
-        if (qpos < S) {
+        if (row_valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c);
           dst[0] = make_uint4(q8[0], q8[1], q8[2], q8[3]);
           dst[1] = make_uint4(q8[4], q8[5], q8[6], q8[7]);
@@ -607,13 +613,14 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   std::memset(&maps, 0, sizeof(maps));
   const long long units = (long long)a.batch * a.kv_heads;
   const size_t kv_plane = (size_t)a.max_seq * D * 2;
+  const int S_kv = a.q_start + a.S;
   bool ok = make_map(&maps.q, a.q, D, a.S, (long long)a.batch * a.kv_heads * G,
                      (size_t)a.S * D * 2, BM);
-  ok = ok && make_map(&maps.k0, a.k[0], D, a.S, units, kv_plane, BN);
-  ok = ok && make_map(&maps.v0, a.v[0], D, a.S, units, kv_plane, BN);
+  ok = ok && make_map(&maps.k0, a.k[0], D, S_kv, units, kv_plane, BN);
+  ok = ok && make_map(&maps.v0, a.v[0], D, S_kv, units, kv_plane, BN);
   if (NSRC == 2) {
-    ok = ok && make_map(&maps.k1, a.k[1], D, a.S, units, kv_plane, BN);
-    ok = ok && make_map(&maps.v1, a.v[1], D, a.S, units, kv_plane, BN);
+    ok = ok && make_map(&maps.k1, a.k[1], D, S_kv, units, kv_plane, BN);
+    ok = ok && make_map(&maps.v1, a.v[1], D, S_kv, units, kv_plane, BN);
   } else {
     maps.k1 = maps.k0;
     maps.v1 = maps.v0;
@@ -629,6 +636,8 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   p.B = a.batch;
   p.H_kv = a.kv_heads;
   p.S = a.S;
+  p.q_start = a.q_start;
+  p.S_kv = S_kv;
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
   const size_t smem = prefill_smem_bytes<D, NSRC, G>();
   auto kern = prefill_kernel<D, NSRC, G>;

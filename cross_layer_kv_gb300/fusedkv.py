@@ -72,6 +72,8 @@ _SIGS = {
                                        ctypes.c_size_t, _P]),
     "fkv_decode_attn_noalloc": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, _P, _P, _P]),
     "fkv_prefill_attn": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P]),
+    "fkv_prefill_attn_chunk": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, _P, _P]),
     "fkv_get_device_status": (ctypes.c_int, [_P, _P]),
     "fkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -255,6 +257,16 @@ class Context:
         m = MODES[mode] if isinstance(mode, str) else int(mode)
         _check(self._lib.fkv_prefill_attn(self.handle, _ptr(q), layer, m, S, _ptr(out),
                                           _stream(stream)), "fkv_prefill_attn")
+        return out
+
+    def fkv_prefill_attn_chunk(self, q, layer: int, mode, q_start: int, C: int, out, stream=None):
+        c = self.cfg
+        shape = (c.batch, c.num_q_heads, C, c.head_dim)
+        self._need(q, shape, self.torch_dtype, "q")
+        self._need(out, shape, self.torch_dtype, "out")
+        m = MODES[mode] if isinstance(mode, str) else int(mode)
+        _check(self._lib.fkv_prefill_attn_chunk(self.handle, _ptr(q), layer, m, q_start, C, _ptr(out),
+                                                _stream(stream)), "fkv_prefill_attn_chunk")
         return out
 
     def fkv_get_device_status(self, stream=None) -> int:

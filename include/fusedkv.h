@@ -166,6 +166,21 @@ fkv_status fkv_decode_attn_noalloc(fkv_ctx* ctx, const void* q, int layer, int m
 fkv_status fkv_prefill_attn(fkv_ctx* ctx, const void* q, int layer, int mode, int S,
                             void* out, void* stream);
 
+/* Causal prefill of a chunk of C prompt positions q_start .. q_start+C-1 over
+ * an existing cache (a long prompt processed in chunks, or a prompt that
+ * extends a cached prefix).  The rows [0, q_start + C) of the caches the call
+ * reads must already hold the prompt's keys and values (fkv_append_kv); query
+ * row i of the chunk sees cache rows t <= q_start + i.
+ * q: device [B, H_q, C, D]; out: device [B, H_q, C, D]; bf16.
+ * fkv_prefill_attn(S) is this call with q_start = 0 and C = S.  The first
+ * token after a prompt of S positions -- the only upper-layer position time to
+ * first token needs (FusedKV slides, backup "prefill skipping has a specific
+ * scope"; reading notes §2.5) -- is one fkv_decode_attn call with length S.
+ * Errors: FKV_ERR_INVALID_ARG unless C >= 1, q_start >= 0 and
+ * q_start + C <= S_max; otherwise as fkv_prefill_attn. */
+fkv_status fkv_prefill_attn_chunk(fkv_ctx* ctx, const void* q, int layer, int mode, int q_start,
+                                  int C, void* out, void* stream);
+
 /* Synchronise the stream, then report and clear the device status word:
  * FKV_OK, FKV_ERR_DEVICE_ARG or FKV_ERR_TIMEOUT (FKV_ERR_CUDA if the sync
  * itself fails). */

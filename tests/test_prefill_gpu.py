@@ -142,3 +142,95 @@ def test_prefill_full_size_sampled(mode):
         assert_close(got[b, h, rows], ref, "bf16", "650M %s b=%d h=%d" % (mode, b, h))
     s.close()
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill over an existing cache
+# ---------------------------------------------------------------------------
+
+def _chunk_oracle(s, q, q_start, bh=None, rows=None):
+    w = s.w
+    ws = ({s.layer: tuple(f64(x) for x in s.weights)} if s.weights else None)
+    n = q_start + q.shape[2]
+    if bh is None:
+        kc = {l: f64(k[:, :, :n]) for l, (k, v) in s.caches.items()}
+        vc = {l: f64(v[:, :, :n]) for l, (k, v) in s.caches.items()}
+        return O.chunk_prefill_attn(f64(q), q_start, s.layer, w.num_layers, s.mode, kc, vc,
+                                    weights=ws)
+    b, h = bh
+    kh = h // w.group
+    kc = {l: f64(k[b:b + 1, kh:kh + 1, :n]) for l, (k, v) in s.caches.items()}
+    vc = {l: f64(v[b:b + 1, kh:kh + 1, :n]) for l, (k, v) in s.caches.items()}
+    if ws:
+        ws = {s.layer: tuple(x[kh:kh + 1] for x in ws[s.layer])}
+    qq = q[b:b + 1, h:h + 1]
+    if rows is not None:
+        # rows of the chunk, each a one-row chunk at its own position
+        return np.stack([O.chunk_prefill_attn(f64(qq[:, :, r:r + 1]), q_start + r, s.layer,
+                                              w.num_layers, s.mode, kc, vc, weights=ws)[0, 0, 0]
+                         for r in rows])
+    return O.chunk_prefill_attn(f64(qq), q_start, s.layer, w.num_layers, s.mode, kc, vc,
+                                weights=ws)[0, 0]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("D", [64, 96])
+def test_prefill_chunks_reassemble_full(mode, D):
+    w = _w(D, 2, 320)
+    S = 300
+    s = PrefillSetup(w, 4, mode, S, seed=6)
+    full = f64(s.run()).copy()
+    parts = []
+    for a, c in ((0, 100), (100, 1), (101, 77), (178, 122)):
+        qc = s.q[:, :, a:a + c].contiguous()
+        oc = torch.empty_like(qc)
+        s.ctx.fkv_prefill_attn_chunk(qc, 4, mode, a, c, oc)
+        parts.append(f64(oc))
+        assert_close(parts[-1], _chunk_oracle(s, qc, a), "bf16", "chunk %d+%d %s" % (a, c, mode))
+    got = np.concatenate(parts, axis=2)
+    assert_close(got, s.oracle(), "bf16", "reassembled %s" % mode)
+    assert np.max(np.abs(got - full)) <= 2e-2
+    s.close()
+
+
+def test_last_prompt_position_is_a_decode_call():
+    """The first generated token needs only the last prompt position in the
+    upper layers: one decode call of length S gives prefill's last row."""
+    w = _w(96, 2, 256)
+    S = 201
+    s = PrefillSetup(w, 4, "fused", S, seed=8)
+    full = f64(s.run())
+    q_last = s.q[:, :, S - 1].contiguous()
+    out = torch.empty_like(q_last)
+    lens = torch.full((w.batch,), S, dtype=torch.int32, device="cuda")
+    ws = s.ctx.workspace()
+    s.ctx.fkv_decode_attn(q_last, 4, "fused", lens, out, ws)
+    assert_close(f64(out), full[:, :, S - 1], "bf16", "decode vs prefill last row")
+    s.close()
+
+
+def test_prefill_chunk_rejects():
+    w = _w(64, 2, 128)
+    s = PrefillSetup(w, 3, "fused", 64)
+    for q_start, c in ((-1, 8), (120, 9), (0, 0)):
+        with pytest.raises(B.FkvError) as e:
+            s.ctx.fkv_prefill_attn_chunk(s.q.data_ptr(), 3, "fused", q_start, c, s.out.data_ptr())
+        assert e.value.status == B.FKV_ERR_INVALID_ARG
+    s.close()
+
+
+@pytest.mark.parametrize("mode", ["fused", "lite"])
+def test_prefill_chunk_full_size_sampled(mode):
+    """650M workload: the second half of an 8192-token prompt as one chunk
+    (q_start = 4096, C = 4096) over the cached first half."""
+    w = synth.M650_PREFILL
+    s = PrefillSetup(w, w.num_layers, mode, 4096, seed=0)
+    q_start = 4096
+    s.ctx.fkv_prefill_attn_chunk(s.q, w.num_layers, mode, q_start, 4096, s.out)
+    got = f64(s.out)
+    rows = [0, 1, 63, 64, 2047, 4095]
+    for b, h in [(0, 0), (3, 15), (2, 7)]:
+        ref = _chunk_oracle(s, s.q, q_start, bh=(b, h), rows=rows)
+        assert_close(got[b, h, rows], ref, "bf16", "650M chunk %s b=%d h=%d" % (mode, b, h))
+    s.close()
+    torch.cuda.empty_cache()
