@@ -46,7 +46,8 @@ import numpy as np
 VANILLA = "vanilla"
 LITE = "lite"
 FUSED = "fused"
-MODES = (VANILLA, LITE, FUSED)
+SCALED = "scaled"   # single-source channel scaling, [Slides] Fig.8 ablation
+MODES = (VANILLA, LITE, FUSED, SCALED)
 
 
 # ---------------------------------------------------------------------------
@@ -77,11 +78,13 @@ def kv_sources(layer: int, num_layers: int, mode: str,
 
     * storage layer (any mode), or vanilla: its own cache;
     * lite ([Slides] Eq.(6)): K^i = K^n, V^i = V^1;
-    * fused ([Slides] Eqs.(4)-(5)): K^i from {K^1, K^n}, V^i from {V^1, V^n}.
+    * fused ([Slides] Eqs.(4)-(5)): K^i from {K^1, K^n}, V^i from {V^1, V^n};
+    * scaled ([Slides] Fig.8, "learnable channel weights" on the Lite
+      sources): K^i = a (.) K^n, V^i = b (.) V^1.
 
     ``k_sources`` / ``v_sources`` override the source layers (the source-layer
-    ablation of [Slides] "Source-layer choice", Table 17); for lite the first
-    entry of each is used.
+    ablation of [Slides] "Source-layer choice", Table 17, and the reversed
+    sharing K^1, V^n of Fig.8); lite and scaled use the first entry of each.
     """
     n = num_storage_layers(num_layers)
     if mode not in MODES:
@@ -90,10 +93,10 @@ def kv_sources(layer: int, num_layers: int, mode: str,
         return {"k": [layer], "v": [layer], "weighted": False}
     ks = tuple(k_sources) if k_sources is not None else None
     vs = tuple(v_sources) if v_sources is not None else None
-    if mode == LITE:
+    if mode in (LITE, SCALED):
         k = ks[0] if ks else n
         v = vs[0] if vs else 1
-        return {"k": [k], "v": [v], "weighted": False}
+        return {"k": [k], "v": [v], "weighted": mode == SCALED}
     return {"k": list(ks) if ks else [1, n], "v": list(vs) if vs else [1, n],
             "weighted": True}
 
@@ -119,6 +122,11 @@ def reconstruct_kv(layer: int, num_layers: int, mode: str,
         return (np.asarray(k_caches[src["k"][0]], dtype=np.float64),
                 np.asarray(v_caches[src["v"][0]], dtype=np.float64))
     a1, an, b1, bn = (np.asarray(w, dtype=np.float64) for w in weights[layer])
+    if len(src["k"]) == 1:
+        # scaled: one source each, weighted by the first key / value weights
+        k = np.asarray(k_caches[src["k"][0]], dtype=np.float64)
+        v = np.asarray(v_caches[src["v"][0]], dtype=np.float64)
+        return a1[None, :, None, :] * k, b1[None, :, None, :] * v
     k1 = np.asarray(k_caches[src["k"][0]], dtype=np.float64)
     kn = np.asarray(k_caches[src["k"][1]], dtype=np.float64)
     v1 = np.asarray(v_caches[src["v"][0]], dtype=np.float64)
@@ -344,6 +352,7 @@ def stored_elements(mode: str, num_layers: int, seq: int, kv_heads: int, head_di
 
 def call_read_elements(layer: int, mode: str, num_layers: int, seq: int, kv_heads: int,
                        head_dim: int, batch: int = 1) -> int:
+    # (scaled reads one K and one V source, like lite)
     """Cache elements one attention call of ``layer`` reads (K and V)."""
     src = kv_sources(layer, num_layers, mode)
     per_source = batch * seq * kv_heads * head_dim

@@ -274,7 +274,7 @@ def test_negative_and_unnormalised_weights_accepted():
     assert np.all(np.isfinite(out))
 
 
-@pytest.mark.parametrize("mode", O.MODES)
+@pytest.mark.parametrize("mode", (O.VANILLA, O.LITE, O.FUSED))
 @pytest.mark.parametrize("layer", [1, 2, 3, 4])
 def test_brute_force_matches_vectorised_decode(mode, layer):
     rng = _rng(13)
@@ -389,7 +389,7 @@ def test_table1_capacity_and_io_ratios():
     g = _golden("table1_capacity_io.json")
     L, S, H, D = 16, 1000, 4, 64
     LSHD = L * S * H * D
-    for m in O.MODES:
+    for m in (O.VANILLA, O.LITE, O.FUSED):   # the three methods of Table 1
         assert O.stored_elements(m, L, S, H, D) / O.stored_elements(O.VANILLA, L, S, H, D) \
             == g["capacity"][m]
         assert O.step_read_elements(m, L, S, H, D) / O.step_read_elements(O.VANILLA, L, S, H, D) \
@@ -467,3 +467,57 @@ def test_chunks_reassemble_full_prefill_and_last_row_is_decode():
     np.testing.assert_allclose(np.concatenate(parts, axis=2), full, atol=1e-12)
     last = O.decode_attn(q[:, :, S - 1], 3, L, O.FUSED, kc, vc, [S], weights=ws)
     np.testing.assert_allclose(full[:, :, S - 1], last, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# source-layer choice ([Slides] Table 17, Fig.8): lite with other sources,
+# reversed sharing, single-source channel scaling
+# --------------------------------------------------------------------------
+
+def test_lite_sources_override_selects_caches():
+    rng = _rng(22)
+    L, B, H_kv, S, D = 8, 1, 2, 12, 8
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2, 3, 4])
+    q = rng.standard_normal((B, 4, D))
+    for ks, vs in (((3,), (1,)), ((1,), (4,)), ((2,), (2,))):
+        got = O.decode_attn(q, 6, L, O.LITE, kc, vc, [S], k_sources=ks, v_sources=vs)
+        ref = _sdpa(q[:, :, None], kc[ks[0]], vc[vs[0]])[:, :, 0]
+        np.testing.assert_allclose(got, ref, atol=1e-12)
+    # the default lite sources are K^n, V^1
+    np.testing.assert_allclose(O.decode_attn(q, 6, L, O.LITE, kc, vc, [S]),
+                               _sdpa(q[:, :, None], kc[4], vc[1])[:, :, 0], atol=1e-12)
+
+
+def test_fused_sources_override():
+    rng = _rng(23)
+    L, B, H_kv, S, D = 8, 1, 1, 10, 4
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2, 3, 4])
+    q = rng.standard_normal((B, 2, D))
+    c = (0.3, 1.7, -0.5, 2.0)
+    ws = {7: tuple(np.full((H_kv, D), x) for x in c)}
+    got = O.decode_attn(q, 7, L, O.FUSED, kc, vc, [S], weights=ws, k_sources=(2, 3),
+                        v_sources=(4, 1))
+    ref = _sdpa(q[:, :, None], c[0] * kc[2] + c[1] * kc[3], c[2] * vc[4] + c[3] * vc[1])[:, :, 0]
+    np.testing.assert_allclose(got, ref, atol=1e-12)
+
+
+def test_scaled_is_lite_with_unit_weights_and_fused_with_zero_second():
+    rng = _rng(24)
+    L, B, H_kv, S, D = 4, 2, 2, 15, 8
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2])
+    q = rng.standard_normal((B, 4, D))
+    ones = tuple(np.ones((H_kv, D)) for _ in range(4))
+    np.testing.assert_array_equal(
+        O.decode_attn(q, 3, L, O.SCALED, kc, vc, [15, 6], weights={3: ones}),
+        O.decode_attn(q, 3, L, O.LITE, kc, vc, [15, 6]))
+    a1, an, b1, bn = _weights(rng, H_kv, D, tie=False)
+    z = np.zeros_like(a1)
+    got = O.decode_attn(q, 3, L, O.SCALED, kc, vc, [15, 6], weights={3: (a1, an, b1, bn)},
+                        k_sources=(1,), v_sources=(2,))
+    ref = O.decode_attn(q, 3, L, O.FUSED, kc, vc, [15, 6], weights={3: (a1, z, b1, z)},
+                        k_sources=(1, 2), v_sources=(2, 1))
+    np.testing.assert_allclose(got, ref, atol=1e-12)
+    # and against SDPA on explicitly scaled caches
+    ks = a1[None, :, None, :] * kc[1]
+    vs = b1[None, :, None, :] * vc[2]
+    np.testing.assert_allclose(got, _sdpa(q[:, :, None], ks, vs, lens=[15, 6])[:, :, 0], atol=1e-12)
