@@ -22,6 +22,8 @@ struct fkv_ctx {
   int* status;    // device status word
   std::vector<void*> k, v;                 // index: layer (1-based)
   std::vector<const float*> w[4];          // a_first, a_second, b_first, b_second
+  std::vector<int> lite_src[2];            // lite / scaled sources: K, V
+  std::vector<int> fused_src[4];           // fused sources: K first, K second, V first, V second
 };
 
 namespace {
@@ -56,7 +58,8 @@ fkv_status check_config(const fkv_config* c) {
 fkv_status resolve_sources(const fkv_ctx* c, int layer, int mode, const void* k[2],
                            const void* v[2], const float* a[2], const float* b[2], int* nsrc) {
   if (layer < 1 || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
-  if (mode != FKV_VANILLA && mode != FKV_LITE && mode != FKV_FUSED) return FKV_ERR_INVALID_ARG;
+  if (mode != FKV_VANILLA && mode != FKV_LITE && mode != FKV_FUSED && mode != FKV_SCALED)
+    return FKV_ERR_INVALID_ARG;
   k[0] = k[1] = v[0] = v[1] = nullptr;
   a[0] = a[1] = b[0] = b[1] = nullptr;
   const int n = c->n;
@@ -68,18 +71,23 @@ fkv_status resolve_sources(const fkv_ctx* c, int layer, int mode, const void* k[
     if (!k[0] || !v[0]) return FKV_ERR_INVALID_ARG;
     return FKV_OK;
   }
-  if (mode == FKV_LITE) {  // K^i = K^n, V^i = V^1
-    k[0] = c->k[n];
-    v[0] = c->v[1];
+  if (mode == FKV_LITE || mode == FKV_SCALED) {  // K^i = K^s, V^i = V^t (default n, 1)
+    k[0] = c->k[c->lite_src[0][layer]];
+    v[0] = c->v[c->lite_src[1][layer]];
     *nsrc = 1;
     if (!k[0] || !v[0]) return FKV_ERR_INVALID_ARG;
+    if (mode == FKV_SCALED) {  // a_first scales K, b_first scales V
+      a[0] = c->w[0][layer];
+      b[0] = c->w[2][layer];
+      if (!a[0] || !b[0]) return FKV_ERR_INVALID_ARG;
+    }
     return FKV_OK;
   }
-  // fused: K^1, K^n with a_first, a_second; V^1, V^n with b_first, b_second
-  k[0] = c->k[1];
-  k[1] = c->k[n];
-  v[0] = c->v[1];
-  v[1] = c->v[n];
+  // fused: K^s1, K^s2 with a_first, a_second; V^t1, V^t2 with b_first, b_second
+  k[0] = c->k[c->fused_src[0][layer]];
+  k[1] = c->k[c->fused_src[1][layer]];
+  v[0] = c->v[c->fused_src[2][layer]];
+  v[1] = c->v[c->fused_src[3][layer]];
   for (int i = 0; i < 2; ++i) {
     a[i] = c->w[i][layer];
     b[i] = c->w[2 + i][layer];
@@ -122,6 +130,12 @@ fkv_status fkv_create(const fkv_config* cfg, fkv_ctx** out) {
   c->k.assign(cfg->num_layers + 1, nullptr);
   c->v.assign(cfg->num_layers + 1, nullptr);
   for (auto& w : c->w) w.assign(cfg->num_layers + 1, nullptr);
+  c->lite_src[0].assign(cfg->num_layers + 1, c->n);  // K^n
+  c->lite_src[1].assign(cfg->num_layers + 1, 1);     // V^1
+  c->fused_src[0].assign(cfg->num_layers + 1, 1);
+  c->fused_src[1].assign(cfg->num_layers + 1, c->n);
+  c->fused_src[2].assign(cfg->num_layers + 1, 1);
+  c->fused_src[3].assign(cfg->num_layers + 1, c->n);
   c->status = nullptr;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
@@ -160,6 +174,28 @@ fkv_status fkv_set_fusion_weights(fkv_ctx* c, int layer, const float* a_first,
     if (!ws[i] || !aligned16(ws[i])) return FKV_ERR_INVALID_ARG;
   for (int i = 0; i < 4; ++i) c->w[i][layer] = ws[i];
   return FKV_OK;
+}
+
+fkv_status fkv_set_sources(fkv_ctx* c, int layer, int mode, int k_first, int k_second,
+                           int v_first, int v_second) {
+  if (!c || layer <= c->n || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
+  auto storage = [&](int l) { return l >= 1 && l <= c->n; };
+  if (mode == FKV_LITE || mode == FKV_SCALED) {
+    if (!storage(k_first) || !storage(v_first)) return FKV_ERR_INVALID_ARG;
+    c->lite_src[0][layer] = k_first;
+    c->lite_src[1][layer] = v_first;
+    return FKV_OK;
+  }
+  if (mode == FKV_FUSED) {
+    if (!storage(k_first) || !storage(k_second) || !storage(v_first) || !storage(v_second))
+      return FKV_ERR_INVALID_ARG;
+    c->fused_src[0][layer] = k_first;
+    c->fused_src[1][layer] = k_second;
+    c->fused_src[2][layer] = v_first;
+    c->fused_src[3][layer] = v_second;
+    return FKV_OK;
+  }
+  return FKV_ERR_INVALID_ARG;
 }
 
 fkv_status fkv_append_kv(fkv_ctx* c, int layer, const void* k_new, const void* v_new,

@@ -4,19 +4,20 @@
 
 namespace fkv {
 
-template <int D, int NSRC>
+template <int D, int NSRC, bool WGT>
 static cudaError_t by_group(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
   switch (a.group) {
-    case 1: return decode_launch_t<float, D, NSRC, 1>(a, pl, s);
-    case 2: return decode_launch_t<float, D, NSRC, 2>(a, pl, s);
-    case 4: return decode_launch_t<float, D, NSRC, 4>(a, pl, s);
+    case 1: return decode_launch_t<float, D, NSRC, WGT, 1>(a, pl, s);
+    case 2: return decode_launch_t<float, D, NSRC, WGT, 2>(a, pl, s);
+    case 4: return decode_launch_t<float, D, NSRC, WGT, 4>(a, pl, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int D>
 static cudaError_t by_src(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
-  return a.nsrc == 2 ? by_group<D, 2>(a, pl, s) : by_group<D, 1>(a, pl, s);
+  if (a.nsrc == 2) return by_group<D, 2, true>(a, pl, s);
+  return a.a[0] ? by_group<D, 1, true>(a, pl, s) : by_group<D, 1, false>(a, pl, s);
 }
 
 cudaError_t decode_launch_f32(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {

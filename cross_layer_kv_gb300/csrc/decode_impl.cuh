@@ -289,7 +289,9 @@ __host__ __device__ constexpr size_t decode_aux_bytes(int warps, int stages, int
   return (size_t)warps * stages * 8 + (size_t)(2 * B + 2) * 4;
 }
 
-template <typename T, int D, int NSRC, int G, int W, int NS, int SB, int VEC>
+// WGT: a single source scaled by channel weights (q (.) a before the dot
+// products, b on the value sums); always set for two sources.
+template <typename T, int D, int NSRC, bool WGT, int G, int W, int NS, int SB, int VEC>
 __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitParams p) {
   using Cfg = DecodeCfg<T, D, NSRC, SB, VEC>;
   constexpr int C = Cfg::C, R = Cfg::R, E = Cfg::E, TR = Cfg::TR, STEPS = Cfg::STEPS;
@@ -439,6 +441,10 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
         const float* an = p.a1 + (size_t)h * D + c * E;
 #pragma unroll
         for (int e = 0; e < E; ++e) { wa0[e] = ap[e]; wa1[e] = an[e]; }
+      } else if (WGT) {  // single source with channel scaling
+        const float* ap = p.a0 + (size_t)h * D + c * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) wa0[e] = ap[e];
       }
 #pragma unroll
       for (int hq = 0; hq < G; ++hq) {
@@ -573,11 +579,16 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
       const long long u = (long long)b * H + h;
       float* rec = p.ws + ((size_t)(w + u) * G) * PS;
       float wb0[E], wb1[E];
+      constexpr bool scale_v = NSRC == 2 || WGT;
       if constexpr (NSRC == 2) {
         const float* bp = p.b0 + (size_t)h * D + c * E;
         const float* bn = p.b1 + (size_t)h * D + c * E;
 #pragma unroll
         for (int e = 0; e < E; ++e) { wb0[e] = bp[e]; wb1[e] = bn[e]; }
+      } else if constexpr (scale_v) {
+        const float* bp = p.b0 + (size_t)h * D + c * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) wb0[e] = bp[e];
       }
 #pragma unroll
       for (int hq = 0; hq < G; ++hq) {
@@ -594,6 +605,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
             if constexpr (NSRC == 2) x1 += __shfl_sync(0xffffffffu, o1[hq][e], k * C + c);
           }
           if constexpr (NSRC == 2) ov[e] = wb0[e] * x0 + wb1[e] * x1;
+          else if constexpr (scale_v) ov[e] = wb0[e] * x0;
           else ov[e] = x0;
         }
         if (g == 0) {
@@ -639,7 +651,7 @@ size_t decode_smem_bytes(int B) {
   return (size_t)S::W * S::NS * Cfg::STAGE_BYTES + decode_aux_bytes(S::W, S::NS, B);
 }
 
-template <typename T, int D, int NSRC, int G>
+template <typename T, int D, int NSRC, bool WGT, int G>
 cudaError_t decode_launch_t(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
   SplitParams sp;
   sp.k0 = a.k[0];
@@ -663,7 +675,7 @@ cudaError_t decode_launch_t(const DecodeArgs& a, const DecodePlan& plan, cudaStr
   sp.S_max = a.max_seq;
   sp.qscale = a.softmax_scale * 1.4426950408889634f;
   using S = DecodeShape<T, D, NSRC, G>;
-  auto kern = decode_split_kernel<T, D, NSRC, G, S::W, S::NS, S::SB, S::VEC>;
+  auto kern = decode_split_kernel<T, D, NSRC, WGT || NSRC == 2, G, S::W, S::NS, S::SB, S::VEC>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem_bytes);
   if (e != cudaSuccess) return e;

@@ -265,7 +265,8 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   uint64_t* s_full = kv_empty + NS;     // [G][2]
   uint64_t* p_full = s_full + 2 * G;    // [G]
   uint64_t* o_done = p_full + G;        // [G]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + G);
+  uint64_t* q_ready = o_done + G;       // Q scaled by a (single-source scaled mode)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x;
@@ -305,15 +306,20 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       mbar_init(&p_full[h], 128);
       mbar_init(&o_done[h], 1);
     }
+    mbar_init(q_ready, 128 * G);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (NSRC == 2) {
+  // one source with channel weights: S = (Q (.) a) K^T, O = (P V) (.) b
+  const bool scaled = NSRC == 1 && p.a0 != nullptr;
+  if (NSRC == 2 || scaled) {
     for (int i = tid; i < D; i += PL::THREADS) {
       sW[i] = p.a0[kh * D + i];
-      sW[D + i] = p.a1[kh * D + i];
       sW[2 * D + i] = p.b0[kh * D + i];
-      sW[3 * D + i] = p.b1[kh * D + i];
+      if (NSRC == 2) {
+        sW[D + i] = p.a1[kh * D + i];
+        sW[3 * D + i] = p.b1[kh * D + i];
+      }
     }
   }
   if (warp == PL::MMA_WARP) tmem_alloc(tmem_slot, TMEM_COLS);
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
           mma_commit(&s_full[2 * h + (j & 1)]);
         }
       };
-      bool ok = wait(bar_q, 0) && wait(&ready[0], 0);
+      bool ok = wait(scaled ? q_ready : bar_q, 0) && wait(&ready[0], 0);
       if (ok) {
         tc_fence_after();
         issue_qk(0);
@@ -456,7 +462,32 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     uint8_t* prow = sP + hh * Cfg::P_BYTES;
     float m_run = -FLT_MAX, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
+    if (scaled) {
+      // this thread's Q row of head hh times a, in place (swizzled chunks)
+      ok = wait(bar_q, 0);
+      uint8_t* qh = sQ + hh * Cfg::Q_BYTES;
+      for (int cb = 0; ok && cb < CB; ++cb) {
+        for (int lc = 0; lc < 4; ++lc) {
+          const int col = cb * SWE + lc * 8;
+          if (col >= D) continue;
+          uint4* pq = reinterpret_cast<uint4*>(qh + cb * BM * SW + swz64(row, lc));
+          float f[8];
+          unpack16<__nv_bfloat16>(*pq, f);
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(f[2 * e] * sW[col + 2 * e],
+                                                      f[2 * e + 1] * sW[col + 2 * e + 1]);
+            o[e] = *reinterpret_cast<uint32_t*>(&v2);
+          }
+          *pq = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_ready);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    for (int j = 0; ok && j < ntiles; ++j) {
       const int n0 = j * BN;
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       if (!__all_sync(0xffffffffu, wait(&s_full[2 * hh + (j & 1)], (uint32_t)(j >> 1) & 1u))) {
@@ -546,6 +577,10 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
         float ov[16];
         tmem_ld16(t_o + c, ov);
         tmem_wait_ld();
+        if (scaled) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ov[e] *= sW[2 * D + c + e];
+        }
         uint32_t q8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {

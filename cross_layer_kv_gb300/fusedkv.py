@@ -25,8 +25,8 @@ FKV_ERR_TIMEOUT = 4
 FKV_ERR_WORKSPACE = 5
 FKV_ERR_DEVICE_ARG = 6
 
-FKV_VANILLA, FKV_LITE, FKV_FUSED = 0, 1, 2
-MODES = {"vanilla": FKV_VANILLA, "lite": FKV_LITE, "fused": FKV_FUSED}
+FKV_VANILLA, FKV_LITE, FKV_FUSED, FKV_SCALED = 0, 1, 2, 3
+MODES = {"vanilla": FKV_VANILLA, "lite": FKV_LITE, "fused": FKV_FUSED, "scaled": FKV_SCALED}
 FKV_BF16, FKV_F32 = 0, 1
 
 # Kernel launches per call: decode = 1 (split + in-kernel merge); append = 1.
@@ -66,6 +66,8 @@ _SIGS = {
     "fkv_destroy": (None, [_P]),
     "fkv_bind_layer_cache": (ctypes.c_int, [_P, ctypes.c_int, _P, _P]),
     "fkv_set_fusion_weights": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P]),
+    "fkv_set_sources": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int]),
     "fkv_append_kv": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, ctypes.c_int, _P]),
     "fkv_decode_workspace_bytes": (ctypes.c_size_t, [_P]),
     "fkv_decode_attn": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, _P, _P, _P,
@@ -201,6 +203,12 @@ class Context:
                                                 _ptr(b_first), _ptr(b_second)),
                "fkv_set_fusion_weights")
         self._keep[("w", layer)] = (a_first, a_second, b_first, b_second)
+
+    def fkv_set_sources(self, layer: int, mode, k_first: int, k_second: int = 0, v_first: int = 0,
+                        v_second: int = 0):
+        m = MODES[mode] if isinstance(mode, str) else int(mode)
+        _check(self._lib.fkv_set_sources(self.handle, layer, m, k_first, k_second, v_first,
+                                         v_second), "fkv_set_sources")
 
     def fkv_append_kv(self, layer: int, k_new, v_new, pos, T: Optional[int] = None, stream=None):
         c = self.cfg

@@ -58,7 +58,14 @@ typedef enum {
   FKV_ERR_DEVICE_ARG = 6    /* device saw a sequence length / position out of range */
 } fkv_status;
 
-typedef enum { FKV_VANILLA = 0, FKV_LITE = 1, FKV_FUSED = 2 } fkv_mode;
+typedef enum {
+  FKV_VANILLA = 0, /* the layer's own cache (Table 1's full-cache baseline) */
+  FKV_LITE = 1,    /* K^i = K^s, V^i = V^t; (s, t) = (n, 1) unless set (Eq.(6)) */
+  FKV_FUSED = 2,   /* K^i = a1 (.) K^s1 + a2 (.) K^s2, likewise V; (1, n) unless set (Eqs.(4)-(5)) */
+  FKV_SCALED = 3   /* K^i = a1 (.) K^s, V^i = b1 (.) V^t on the Lite sources: the
+                      single-source learnable channel scaling of the FusedKV
+                      slides' Fig.8 ablation */
+} fkv_mode;
 
 typedef enum { FKV_BF16 = 0, FKV_F32 = 1 } fkv_dtype;
 
@@ -105,6 +112,17 @@ fkv_status fkv_set_fusion_weights(fkv_ctx* ctx, int layer, const float* a_first,
                                   const float* a_second, const float* b_first,
                                   const float* b_second);
 
+/* Choose the stored layers an upper layer n < layer <= L reconstructs from
+ * (FusedKV slides, "source-layer choice", Table 17, and the reversed sharing
+ * K^1, V^n of Fig.8).  For mode FKV_LITE or FKV_SCALED, K comes from layer
+ * k_first and V from layer v_first (k_second and v_second are ignored); for
+ * FKV_FUSED, K from layers k_first and k_second (weighted by a_first,
+ * a_second) and V from v_first and v_second (b_first, b_second).  Every
+ * source must be a storage layer 1..n.  Defaults: Lite / scaled (n, 1),
+ * fused (1, n, 1, n).  The caches must be bound before a call reads them. */
+fkv_status fkv_set_sources(fkv_ctx* ctx, int layer, int mode, int k_first, int k_second,
+                           int v_first, int v_second);
+
 /* Write the post-RoPE K/V of T new tokens into a layer's cache (the storage
  * caches take the new token before the upper layers attend; reading notes
  * §2.3).  k_new, v_new: device [B, H_kv, T, D] in the context dtype.
@@ -129,7 +147,8 @@ size_t fkv_decode_workspace_bytes(const fkv_ctx* ctx);
  * mode: for storage layers every mode is plain attention over the layer's own
  * cache; for upper layers FKV_VANILLA reads the layer's own cache (needs
  * store_upper), FKV_LITE reads K^n and V^1, FKV_FUSED reads K^1, K^n, V^1, V^n
- * with the layer's weights and fuses them in registers.
+ * with the layer's weights and fuses them in registers, FKV_SCALED reads K^n
+ * and V^1 scaled by a_first and b_first (sources as set by fkv_set_sources).
  * workspace: device, at least fkv_decode_workspace_bytes(ctx) bytes. */
 fkv_status fkv_decode_attn(fkv_ctx* ctx, const void* q, int layer, int mode,
                            const int32_t* seq_lens, void* out, void* workspace,

@@ -46,9 +46,7 @@ def layers_read(w, layer, mode):
     n = w.n
     if layer <= n or mode == "vanilla":
         return [layer]
-    if mode == "lite":
-        return sorted({1, n})
-    return sorted({1, n})
+    return sorted({1, n})   # lite, scaled and fused default sources
 
 
 class DecodeSetup:
@@ -56,12 +54,17 @@ class DecodeSetup:
     to a library context."""
 
     def __init__(self, w, layer, modes, seed=0, device="cuda", lens=None, decode_ctas=0,
-                 weight_std=0.3, tie_keys=True):
+                 weight_std=0.3, tie_keys=True, sources=None):
+        """``sources``: {mode: (k_first, k_second, v_first, v_second)} to
+        reconstruct from other storage layers (all storage layers are bound)."""
         import cross_layer_kv_gb300 as fkv
         from cross_layer_kv_gb300 import synth
         self.w = w
         self.layer = layer
+        self.sources = dict(sources or {})
         need = sorted({l for m in modes for l in layers_read(w, layer, m)})
+        if self.sources:
+            need = sorted(set(need) | set(range(1, w.n + 1)))
         store_upper = any(l > w.n for l in need)
         self.ctx = fkv.Context(w.num_layers, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim,
                                w.dtype, store_upper=store_upper, decode_ctas=decode_ctas)
@@ -75,6 +78,8 @@ class DecodeSetup:
             self.weights = synth.make_weights(w, layer, seed, device, tie_keys=tie_keys,
                                               std=weight_std)
             self.ctx.fkv_set_fusion_weights(layer, *self.weights)
+        for m, src in self.sources.items():
+            self.ctx.fkv_set_sources(layer, m, *src)
         self.q = synth.make_query(w, layer, seed, device)
         if lens is None:
             self.lens = synth.make_seq_lens(w, seed, device)
@@ -87,18 +92,27 @@ class DecodeSetup:
         self.ctx.fkv_decode_attn(self.q, self.layer, mode, self.lens, self.out, self.ws)
         return self.out
 
+    def source_kwargs(self, mode):
+        src = self.sources.get(mode)
+        if not src:
+            return {}
+        if mode == "fused":
+            return {"k_sources": (src[0], src[1]), "v_sources": (src[2], src[3])}
+        return {"k_sources": (src[0],), "v_sources": (src[2],)}
+
     def oracle(self, mode, pairs=None):
         """float64 oracle output, all (b, hq) or the listed pairs."""
         import oracle as O
         w = self.w
         lens = self.lens.cpu().tolist()
         G = w.group
+        sk = self.source_kwargs(mode)
         if pairs is None:
             kc = {l: f64(k) for l, (k, v) in self.caches.items()}
             vc = {l: f64(v) for l, (k, v) in self.caches.items()}
             ws = {self.layer: tuple(f64(x) for x in self.weights)} if self.weights else None
             return O.decode_attn(f64(self.q), self.layer, w.num_layers, mode, kc, vc, lens,
-                                 weights=ws)
+                                 weights=ws, **sk)
         out = []
         for b, hq in pairs:
             kh = hq // G
@@ -108,7 +122,7 @@ class DecodeSetup:
             ws = ({self.layer: tuple(f64(x[kh:kh + 1]) for x in self.weights)}
                   if self.weights else None)
             o = O.decode_attn(f64(self.q[b:b + 1, hq:hq + 1]), self.layer, w.num_layers, mode,
-                              kc, vc, [n], weights=ws)
+                              kc, vc, [n], weights=ws, **sk)
             out.append(o[0, 0])
         return np.stack(out)
 

@@ -17,6 +17,7 @@ from parity import DecodeSetup, assert_close, f64
 pytestmark = pytest.mark.gpu
 
 MODES = ("vanilla", "lite", "fused")
+ALL_MODES = MODES + ("scaled",)
 
 
 @pytest.fixture(autouse=True)
@@ -188,4 +189,46 @@ def test_workspace_garbage_and_reuse():
         assert_close(f64(s.run("fused")), ref_f, "bf16", "fused, dirty workspace")
         assert_close(f64(s.run("lite")), ref_l, "bf16", "lite, dirty workspace")
     assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    s.close()
+
+
+
+# ---------------------------------------------------------------------------
+# source-layer choice and single-source channel scaling (FusedKV slides,
+# Table 17 and Fig.8)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [64, 80, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_scaled_mode_default_sources(D, dtype):
+    w = _small(D, 2, dtype=dtype, S=600, Bt=3)
+    s = DecodeSetup(w, 6, ["scaled"], seed=14, lens=[600, 300, 5])
+    assert_close(f64(s.run("scaled")), s.oracle("scaled"), dtype, "scaled D=%d" % D)
+    s.close()
+
+
+@pytest.mark.parametrize("mode,src", [
+    ("lite", (2, 0, 3, 0)),       # middle-layer K, V source 3
+    ("lite", (1, 0, 3, 0)),       # reversed sharing K^1, V^n (n = 3)
+    ("scaled", (2, 0, 1, 0)),
+    ("fused", (2, 3, 3, 1)),
+    ("fused", (3, 3, 1, 1)),      # both weights on one layer
+])
+def test_custom_sources(mode, src):
+    w = _small(64, 2, S=512, Bt=2)   # 6 layers, storage 1..3
+    s = DecodeSetup(w, 5, [mode], seed=15, lens=[512, 100], sources={mode: src})
+    assert_close(f64(s.run(mode)), s.oracle(mode), "bf16", "%s %s" % (mode, src))
+    s.close()
+
+
+def test_set_sources_rejects_non_storage_layers():
+    w = _small(64, 2, S=64, Bt=1)
+    s = DecodeSetup(w, 5, ["lite"], seed=16, lens=[64])
+    for args in (("lite", 4, 0, 1, 0), ("fused", 1, 5, 1, 1), ("vanilla", 1, 1, 1, 1),
+                 ("lite", 0, 0, 1, 0)):
+        with pytest.raises(B.FkvError) as e:
+            s.ctx.fkv_set_sources(5, *args)
+        assert e.value.status == B.FKV_ERR_INVALID_ARG
+    with pytest.raises(B.FkvError):
+        s.ctx.fkv_set_sources(2, "lite", 1, 0, 1, 0)   # a storage layer has no sources
     s.close()

@@ -24,10 +24,13 @@ def _cuda():
 
 
 class PrefillSetup:
-    def __init__(self, w, layer, mode, S, seed=0, tie_keys=True):
+    def __init__(self, w, layer, mode, S, seed=0, tie_keys=True, sources=None):
         self.w, self.layer, self.mode, self.S = w, layer, mode, S
+        self.sources = sources
         n = w.n
         need = [layer] if (layer <= n or mode == "vanilla") else sorted({1, n})
+        if sources:
+            need = sorted(set(need) | set(range(1, n + 1)))
         self.ctx = B.Context(w.num_layers, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim,
                              "bf16", store_upper=any(l > n for l in need))
         self.caches = {}
@@ -39,6 +42,8 @@ class PrefillSetup:
         if layer > n:
             self.weights = synth.make_weights(w, layer, seed, "cuda", tie_keys=tie_keys)
             self.ctx.fkv_set_fusion_weights(layer, *self.weights)
+        if sources:
+            self.ctx.fkv_set_sources(layer, mode, *sources)
         g = torch.Generator(device="cuda").manual_seed(seed + 99)
         self.q = torch.randn(w.batch, w.q_heads, S, w.head_dim, generator=g,
                              device="cuda").to(torch.bfloat16)
@@ -48,15 +53,24 @@ class PrefillSetup:
         self.ctx.fkv_prefill_attn(self.q, self.layer, self.mode, self.S, self.out)
         return self.out
 
+    def source_kwargs(self):
+        src = self.sources
+        if not src:
+            return {}
+        if self.mode == "fused":
+            return {"k_sources": (src[0], src[1]), "v_sources": (src[2], src[3])}
+        return {"k_sources": (src[0],), "v_sources": (src[2],)}
+
     def oracle(self, bh=None, rows=None):
         w = self.w
         G = w.group
+        sk = self.source_kwargs()
         ws = ({self.layer: tuple(f64(x) for x in self.weights)} if self.weights else None)
         if bh is None:
             kc = {l: f64(k) for l, (k, v) in self.caches.items()}
             vc = {l: f64(v) for l, (k, v) in self.caches.items()}
             return O.prefill_attn(f64(self.q), self.layer, w.num_layers, self.mode, kc, vc,
-                                  weights=ws, rows=rows)
+                                  weights=ws, rows=rows, **sk)
         b, h = bh
         kh = h // G
         kc = {l: f64(k[b:b + 1, kh:kh + 1, :self.S]) for l, (k, v) in self.caches.items()}
@@ -64,7 +78,7 @@ class PrefillSetup:
         if ws:
             ws = {self.layer: tuple(x[kh:kh + 1] for x in ws[self.layer])}
         return O.prefill_attn(f64(self.q[b:b + 1, h:h + 1]), self.layer, w.num_layers, self.mode,
-                              kc, vc, weights=ws, rows=rows)[0, 0]
+                              kc, vc, weights=ws, rows=rows, **sk)[0, 0]
 
     def close(self):
         self.ctx.close()
@@ -234,3 +248,15 @@ def test_prefill_chunk_full_size_sampled(mode):
         assert_close(got[b, h, rows], ref, "bf16", "650M chunk %s b=%d h=%d" % (mode, b, h))
     s.close()
     torch.cuda.empty_cache()
+
+
+
+@pytest.mark.parametrize("mode,src,D", [
+    ("scaled", None, 64), ("scaled", None, 96), ("scaled", (2, 0, 1, 0), 80),
+    ("lite", (1, 0, 3, 0), 64), ("fused", (2, 3, 3, 1), 96),
+])
+def test_prefill_sources_and_scaled(mode, src, D):
+    w = synth.Workload("p6", 6, 2, 260, 4, 2, D, "bf16")   # storage layers 1..3
+    s = PrefillSetup(w, 5, mode, 250, seed=9, sources=src)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "prefill %s %s D=%d" % (mode, src, D))
+    s.close()
