@@ -23,7 +23,9 @@
 //    tensor cores work while the softmax warps run;
 //  * one softmax warpgroup per head: each thread owns one query row (one TMEM
 //    lane), reads its S row with tcgen05.ld, applies the causal mask and the
-//    online (base-2) softmax and writes P_h (bf16) to swizzled shared memory;
+//    online (base-2) softmax and writes P_h (bf16) back over that S tile with
+//    tcgen05.st; the PV product takes its A operand from tensor memory, so P
+//    never touches shared memory;
 //    O is rescaled in tensor memory only when the running max grows by more
 //    than 2^8.
 //  * Every wait is bounded; a wait that runs out sets an abort flag that
@@ -112,6 +114,31 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
       "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
       "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
       "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane <- v.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// D (TMEM) (+)= A (TMEM, 128 lanes x K packed bf16) * B (shared memory).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -213,7 +240,7 @@ template <int D, int NSRC, int G>
 struct PrefillPlan {
   using Cfg = PrefillCfg<D>;
   static constexpr int STAGE = 2 * NSRC * Cfg::KV_BYTES;
-  static constexpr int FIXED = G * Cfg::Q_BYTES + G * Cfg::P_BYTES + 4 * D * 4 + AUX_BYTES + 512;
+  static constexpr int FIXED = G * Cfg::Q_BYTES + 4 * D * 4 + AUX_BYTES + 512;
   static constexpr int NS_FIT = (SMEM_LIMIT - FIXED) / STAGE;
   static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;   // K/V ring stages
   static constexpr int SOFTMAX_WARPS = 4 * G;
@@ -255,8 +282,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
                                              ~uintptr_t(511));
   uint8_t* sQ = smem;
   uint8_t* sKV = sQ + G * Cfg::Q_BYTES;
-  uint8_t* sP = sKV + NS * PL::STAGE;
-  float* sW = reinterpret_cast<float*>(sP + G * Cfg::P_BYTES);
+  float* sW = reinterpret_cast<float*>(sKV + NS * PL::STAGE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sW + 4 * D);
   uint64_t* bar_q = bars;
   uint64_t* kv_full = bars + 1;
@@ -389,12 +415,14 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
         for (int h = 0; h < G; ++h) {
           if (!wait(&p_full[h], (uint32_t)j & 1u)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t pbase = smem_u32(sP + h * Cfg::P_BYTES);
+          // P_h (bf16, two per column) sits in the first BN/2 columns of the
+          // S tile it was computed from
+          const uint32_t ptmem = tmem + h * HEAD_COLS + (j & 1) * BN;
 #pragma unroll
           for (int k = 0; k < BN / 16; ++k) {
-            const uint64_t ad = sdesc(pbase + (k >> 1) * BM * SW + (k & 1) * 32, 16, 8 * SW);
             const uint64_t bd = sdesc(vbase + k * 16 * SW, BN * SW, 8 * SW);
-            mma_bf16(tmem + h * HEAD_COLS + 2 * BN, ad, bd, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + h * HEAD_COLS + 2 * BN, ptmem + k * 8, bd, IDESC_PV,
+                        (j > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&o_done[h]);
         }
@@ -459,7 +487,6 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const uint32_t t_head = tmem + lane_addr + hh * HEAD_COLS;
     const uint32_t t_o = t_head + 2 * BN;
-    uint8_t* prow = sP + hh * Cfg::P_BYTES;
     float m_run = -FLT_MAX, l_run = 0.f;
     bool ok = true;
     if (scaled) {
@@ -557,14 +584,12 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
           tmem_wait_st();
         }
       }
-#pragma unroll
-      for (int c = 0; c < BN; c += 8) {
-        const int blk = c / SWE, lc = (c % SWE) / 8;
-        *reinterpret_cast<uint4*>(prow + blk * BM * SW + swz64(row, lc)) =
-            make_uint4(pk[c / 2], pk[c / 2 + 1], pk[c / 2 + 2], pk[c / 2 + 3]);
-      }
+      // P over the S tile just read (its first BN/2 columns): the MMA reads it
+      // from tensor memory as the A operand of O += P V
+      static_assert(BN / 2 == 32, "one 32-column store per row");
+      tmem_st32(t_head + (j & 1) * BN, pk);
+      tmem_wait_st();
       tc_fence_before();
-      fence_proxy_async_smem();
       mbar_arrive(&p_full[hh]);
     }
     if (ok && __all_sync(0xffffffffu, wait(&o_done[hh], (uint32_t)(ntiles - 1) & 1u))) {
