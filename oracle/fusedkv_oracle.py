@@ -163,11 +163,14 @@ def attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndar
 
 
 def decode_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
-                     seq_lens: Sequence[int], scale: Optional[float] = None) -> np.ndarray:
+                     seq_lens: Sequence[int], scale: Optional[float] = None,
+                     window: int = 0) -> np.ndarray:
     """One decode step of GQA softmax attention.
 
     q ``[B, H_q, D]``; k, v ``[B, H_kv, S, D]``; each sequence b attends over
-    positions ``[0, seq_lens[b])``.  Query head h reads KV head h // G.
+    positions ``[0, seq_lens[b])``, or only the last ``window`` of them for a
+    sliding-window layer (window > 0; the hybrid SWA layers of [Slides]
+    "MoE and hybrid SWA").  Query head h reads KV head h // G.
     Returns float64 ``[B, H_q, D]``.
     """
     B, H_q, D = q.shape
@@ -182,21 +185,22 @@ def decode_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
         n = int(seq_lens[b])
         if not 1 <= n <= k.shape[2]:
             raise ValueError("sequence length out of range")
+        lo = max(0, n - window) if window > 0 else 0
         for h in range(H_q):
             kv = h // G
-            out[b, h] = attend(q[b, h], k[b, kv, :n], v[b, kv, :n], scale)
+            out[b, h] = attend(q[b, h], k[b, kv, lo:n], v[b, kv, lo:n], scale)
     return out
 
 
 def prefill_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
                       scale: Optional[float] = None,
-                      rows: Optional[Sequence[int]] = None) -> np.ndarray:
+                      rows: Optional[Sequence[int]] = None, window: int = 0) -> np.ndarray:
     """Causal GQA attention over a prompt that starts at position 0.
 
     q ``[B, H_q, S, D]``; k, v ``[B, H_kv, >=S, D]``.  Query position m sees
-    key positions t <= m (inclusive diagonal).  With ``rows`` given, only
-    those query positions are computed and the result is
-    ``[B, H_q, len(rows), D]``.
+    key positions t <= m (inclusive diagonal), and with window > 0 only
+    t > m - window.  With ``rows`` given, only those query positions are
+    computed and the result is ``[B, H_q, len(rows), D]``.
     """
     B, H_q, S, D = q.shape
     H_kv = k.shape[1]
@@ -212,31 +216,33 @@ def prefill_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
             vv = np.asarray(v[b, kv], dtype=np.float64)
             qq = np.asarray(q[b, h], dtype=np.float64)
             for i, m in enumerate(rows):
-                out[b, h, i] = attend(qq[m], kk[:m + 1], vv[:m + 1], scale)
+                lo = max(0, m + 1 - window) if window > 0 else 0
+                out[b, h, i] = attend(qq[m], kk[lo:m + 1], vv[lo:m + 1], scale)
     return out
 
 
 def decode_attn(q, layer, num_layers, mode, k_caches, v_caches, seq_lens,
-                weights=None, scale=None, k_sources=None, v_sources=None):
+                weights=None, scale=None, k_sources=None, v_sources=None, window=0):
     """A decode attention call of one layer: reconstruct, then attend."""
     k_i, v_i = reconstruct_kv(layer, num_layers, mode, k_caches, v_caches,
                               weights, k_sources, v_sources)
-    return decode_attention(q, k_i, v_i, seq_lens, scale)
+    return decode_attention(q, k_i, v_i, seq_lens, scale, window)
 
 
 def prefill_attn(q, layer, num_layers, mode, k_caches, v_caches,
-                 weights=None, scale=None, rows=None, k_sources=None, v_sources=None):
+                 weights=None, scale=None, rows=None, k_sources=None, v_sources=None,
+                 window=0):
     """A causal prefill attention call of one layer: reconstruct, then attend."""
     S = q.shape[2]
     k_i, v_i = reconstruct_kv(layer, num_layers, mode,
                               {l: c[:, :, :S] for l, c in k_caches.items()},
                               {l: c[:, :, :S] for l, c in v_caches.items()},
                               weights, k_sources, v_sources)
-    return prefill_attention(q, k_i, v_i, scale, rows)
+    return prefill_attention(q, k_i, v_i, scale, rows, window)
 
 
 def chunk_prefill_attention(q: np.ndarray, q_start: int, k: np.ndarray, v: np.ndarray,
-                            scale: Optional[float] = None) -> np.ndarray:
+                            scale: Optional[float] = None, window: int = 0) -> np.ndarray:
     """Causal attention of a chunk of queries over an existing cache.
 
     q ``[B, H_q, C, D]`` holds the queries of positions q_start .. q_start+C-1;
@@ -256,12 +262,13 @@ def chunk_prefill_attention(q: np.ndarray, q_start: int, k: np.ndarray, v: np.nd
             kv = h // G
             for i in range(C):
                 n = q_start + i + 1
-                out[b, h, i] = attend(q[b, h, i], k[b, kv, :n], v[b, kv, :n], scale)
+                lo = max(0, n - window) if window > 0 else 0
+                out[b, h, i] = attend(q[b, h, i], k[b, kv, lo:n], v[b, kv, lo:n], scale)
     return out
 
 
 def chunk_prefill_attn(q, q_start, layer, num_layers, mode, k_caches, v_caches, weights=None,
-                       scale=None, k_sources=None, v_sources=None):
+                       scale=None, k_sources=None, v_sources=None, window=0):
     """A chunked causal prefill call of one layer: reconstruct rows
     [0, q_start + C), then attend."""
     n = q_start + q.shape[2]
@@ -269,7 +276,7 @@ def chunk_prefill_attn(q, q_start, layer, num_layers, mode, k_caches, v_caches, 
                               {l: c[:, :, :n] for l, c in k_caches.items()},
                               {l: c[:, :, :n] for l, c in v_caches.items()},
                               weights, k_sources, v_sources)
-    return chunk_prefill_attention(q, q_start, k_i, v_i, scale)
+    return chunk_prefill_attention(q, q_start, k_i, v_i, scale, window)
 
 
 # ---------------------------------------------------------------------------

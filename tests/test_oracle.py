@@ -521,3 +521,47 @@ def test_scaled_is_lite_with_unit_weights_and_fused_with_zero_second():
     ks = a1[None, :, None, :] * kc[1]
     vs = b1[None, :, None, :] * vc[2]
     np.testing.assert_allclose(got, _sdpa(q[:, :, None], ks, vs, lens=[15, 6])[:, :, 0], atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# sliding-window layers (hybrid SWA of [Slides] "MoE and hybrid SWA": window
+# 512, three window layers per full-attention layer)
+# --------------------------------------------------------------------------
+
+def test_window_decode_matches_sdpa_on_last_rows_and_special_cases():
+    rng = _rng(25)
+    B, H_kv, S, D = 3, 2, 40, 8
+    q = rng.standard_normal((B, 4, D))
+    k = rng.standard_normal((B, H_kv, S, D))
+    v = rng.standard_normal((B, H_kv, S, D))
+    lens = [40, 7, 25]
+    for W in (1, 5, 7, 64):
+        got = O.decode_attention(q, k, v, lens, window=W)
+        for b, n in enumerate(lens):
+            lo = max(0, n - W)
+            ref = _sdpa(q[b:b + 1, :, None], k[b:b + 1, :, lo:n], v[b:b + 1, :, lo:n])[0, :, 0]
+            np.testing.assert_allclose(got[b], ref, atol=1e-12)
+    # window 1: the newest value row; a window at least len: full attention
+    w1 = O.decode_attention(q, k, v, lens, window=1)
+    for b, n in enumerate(lens):
+        np.testing.assert_array_equal(w1[b, 0], v[b, 0, n - 1])
+    np.testing.assert_array_equal(O.decode_attention(q, k, v, lens, window=40),
+                                  O.decode_attention(q, k, v, lens))
+
+
+def test_window_prefill_matches_sdpa_band_mask():
+    rng = _rng(26)
+    B, H_kv, S, D, W = 1, 2, 30, 8, 6
+    q = rng.standard_normal((B, 4, S, D))
+    k = rng.standard_normal((B, H_kv, S, D))
+    v = rng.standard_normal((B, H_kv, S, D))
+    got = O.prefill_attention(q, k, v, window=W)
+    mask = torch.tensor([[m - W < t <= m for t in range(S)] for m in range(S)])
+    qt = torch.from_numpy(q)
+    kt = torch.from_numpy(k).repeat_interleave(2, dim=1)
+    vt = torch.from_numpy(v).repeat_interleave(2, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask).numpy()
+    np.testing.assert_allclose(got, ref, atol=1e-12)
+    # chunked, windowed: rows of the full windowed prefill
+    part = O.chunk_prefill_attention(q[:, :, 11:20], 11, k, v, window=W)
+    np.testing.assert_allclose(part, got[:, :, 11:20], atol=1e-12)
