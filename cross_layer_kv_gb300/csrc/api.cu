@@ -24,6 +24,7 @@ struct fkv_ctx {
   std::vector<const float*> w[4];          // a_first, a_second, b_first, b_second
   std::vector<int> lite_src[2];            // lite / scaled sources: K, V
   std::vector<int> fused_src[4];           // fused sources: K first, K second, V first, V second
+  std::vector<int> window;                 // sliding window per layer (0: full attention)
 };
 
 namespace {
@@ -130,6 +131,7 @@ fkv_status fkv_create(const fkv_config* cfg, fkv_ctx** out) {
   c->k.assign(cfg->num_layers + 1, nullptr);
   c->v.assign(cfg->num_layers + 1, nullptr);
   for (auto& w : c->w) w.assign(cfg->num_layers + 1, nullptr);
+  c->window.assign(cfg->num_layers + 1, 0);
   c->lite_src[0].assign(cfg->num_layers + 1, c->n);  // K^n
   c->lite_src[1].assign(cfg->num_layers + 1, 1);     // V^1
   c->fused_src[0].assign(cfg->num_layers + 1, 1);
@@ -198,6 +200,12 @@ fkv_status fkv_set_sources(fkv_ctx* c, int layer, int mode, int k_first, int k_s
   return FKV_ERR_INVALID_ARG;
 }
 
+fkv_status fkv_set_window(fkv_ctx* c, int layer, int window) {
+  if (!c || layer < 1 || layer > c->cfg.num_layers || window < 0) return FKV_ERR_INVALID_ARG;
+  c->window[layer] = window;
+  return FKV_OK;
+}
+
 fkv_status fkv_append_kv(fkv_ctx* c, int layer, const void* k_new, const void* v_new,
                          const int32_t* pos, int T, void* stream) {
   if (!c || layer < 1 || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
@@ -256,6 +264,7 @@ fkv_status fkv_decode_attn(fkv_ctx* c, const void* q, int layer, int mode,
   d.out = out;
   d.seq_lens = seq_lens;
   d.workspace = static_cast<float*>(workspace);
+  d.window = c->window[layer];
   unsigned ep = g_decode_epoch.fetch_add(1);
   if (ep == 0) ep = g_decode_epoch.fetch_add(1);
   d.epoch = ep;
@@ -280,6 +289,7 @@ fkv_status fkv_prefill_attn_chunk(fkv_ctx* c, const void* q, int layer, int mode
   if (S < 1 || q_start < 0 || (long long)q_start + S > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return FKV_ERR_INVALID_ARG;
   p.q_start = q_start;
+  p.window = c->window[layer];
   p.q = q;
   p.out = out;
   p.status = c->status;

@@ -127,6 +127,7 @@ struct SplitParams {
   unsigned long long* counters;    // one arrival word per (b, kh) unit
   int* status;
   int B, H_kv, S_max;
+  int window;                      // > 0: only the last `window` rows of each sequence
   unsigned epoch;                  // tag of this call's arrivals
   float qscale;  // softmax scale * log2(e)
 };
@@ -286,7 +287,7 @@ __device__ __forceinline__ void merge_unit(const float* ws, T* out, long long u,
 
 // Shared-memory bytes of the split kernel besides the stages.
 __host__ __device__ constexpr size_t decode_aux_bytes(int warps, int stages, int B) {
-  return (size_t)warps * stages * 8 + (size_t)(2 * B + 2) * 4;
+  return (size_t)warps * stages * 8 + (size_t)(3 * B + 2) * 4;
 }
 
 // WGT: a single source scaled by channel weights (q (.) a before the dot
@@ -301,8 +302,9 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
 
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)W * NS * STAGE);
-  int* lens = reinterpret_cast<int*>(bars + W * NS);
-  int* pre = lens + p.B;  // pre[b] = sum_{b' < b} lens[b'], B + 1 entries
+  int* lens = reinterpret_cast<int*>(bars + W * NS);  // rows attended per sequence
+  int* pre = lens + p.B;      // pre[b] = sum_{b' < b} lens[b'], B + 1 entries
+  int* first = pre + p.B + 1; // cache row of each sequence's first attended row
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -322,7 +324,10 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
       if (blockIdx.x == 0) flag_status(p.status, kDevBadArg);
       L = L < 0 ? 0 : (L > p.S_max ? p.S_max : L);
     }
-    lens[i] = L;
+    // a sliding-window layer attends to the last `window` rows only
+    const int Le = p.window > 0 && L > p.window ? p.window : L;
+    lens[i] = Le;
+    first[i] = L - Le;
   }
   __syncthreads();
   if (warp == 0) {
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
 
   auto issue = [&](int stage, int b, int h, int t, int n) {
     if (lane == 0) {
-      const size_t off = ((size_t)b * H + h) * row_stride_u + (size_t)t * ROWB;
+      const size_t off = ((size_t)b * H + h) * row_stride_u + (size_t)(first[b] + t) * ROWB;
       const uint32_t bytes = (uint32_t)n * ROWB;
       uint8_t* dst = ring + (size_t)stage * STAGE;
       uint64_t* bar = &wbars[stage];
@@ -673,6 +678,7 @@ cudaError_t decode_launch_t(const DecodeArgs& a, const DecodePlan& plan, cudaStr
   sp.B = a.batch;
   sp.H_kv = a.kv_heads;
   sp.S_max = a.max_seq;
+  sp.window = a.window;
   sp.qscale = a.softmax_scale * 1.4426950408889634f;
   using S = DecodeShape<T, D, NSRC, G>;
   auto kern = decode_split_kernel<T, D, NSRC, WGT || NSRC == 2, G, S::W, S::NS, S::SB, S::VEC>;

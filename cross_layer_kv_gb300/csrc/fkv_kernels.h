@@ -26,6 +26,7 @@ struct DecodeArgs {
   int is_f32;
   float softmax_scale;
   int num_ctas;              // split grid (0 = library default)
+  int window;                // > 0: attend only to the last `window` rows
   unsigned epoch;            // distinct per call (tags the unit arrival counts)
 };
 
@@ -88,6 +89,7 @@ struct PrefillArgs {
   int* status;
   int batch, kv_heads, group, max_seq, head_dim, S;
   int q_start;     // cache position of query row 0 (0 for a whole prompt)
+  int window;      // > 0: sliding window of that many positions
   int nsrc;
   float softmax_scale;
 };

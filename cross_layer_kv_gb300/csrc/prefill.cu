@@ -35,6 +35,7 @@
 #include <cudaTypedefs.h>
 
 #include <cfloat>
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -224,6 +225,7 @@ struct PrefillParams {
   int S;        // query rows of this call (the chunk length C)
   int q_start;  // cache position of the first query row
   int S_kv;     // key rows attended: q_start + C
+  int window;   // > 0: a query at position m sees only keys t > m - window
   float scale_log2;
 };
 
@@ -304,7 +306,11 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   const int S = p.S;                   // query rows
   const int S_kv = p.S_kv;             // key rows
   const int pos0 = p.q_start + m0;     // cache position of query row m0
-  const int ntiles = (min(pos0 + BM, S_kv) + BN - 1) / BN;
+  const int W = p.window;
+  // key tiles [j0, j_end): up to the last query's position, from the first
+  // query's window start (sliding-window layers skip the tiles before it)
+  const int j0 = W > 0 ? max(0, pos0 - W + 1) / BN : 0;
+  const int ntiles = (min(pos0 + BM, S_kv) + BN - 1) / BN - j0;   // tiles processed
   const int H_q = p.H_kv * G;
 
   auto stage_k = [&](int s, int src) { return sKV + (size_t)s * PL::STAGE + (size_t)src * Cfg::KV_BYTES; };
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % NS, u = j / NS;
         if (u > 0 && !wait(&kv_empty[s], (uint32_t)(u - 1) & 1u)) break;
-        const int n0 = j * BN;
+        const int n0 = (j0 + j) * BN;
         mbar_arrive_expect_tx(&kv_full[s], PL::STAGE);
         for (int cb = 0; cb < CB; ++cb) {
           tma_load_3d(stage_k(s, 0) + cb * BN * SW, &maps.k0, cb * SWE, n0, unit, &kv_full[s]);
@@ -515,7 +521,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
     }
     for (int j = 0; ok && j < ntiles; ++j) {
-      const int n0 = j * BN;
+      const int n0 = (j0 + j) * BN;
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       if (!__all_sync(0xffffffffu, wait(&s_full[2 * hh + (j & 1)], (uint32_t)(j >> 1) & 1u))) {
         ok = false;
@@ -526,12 +532,15 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < BN; c += 16) tmem_ld16(t_head + (j & 1) * BN + c, sv + c);
       tmem_wait_ld();
-      const bool diag = n0 + BN > pos0 || n0 + BN > S_kv;   // warp-uniform
+      // masking needed: the causal diagonal, the key extent, or (window) the
+      // lowest row-window start of the tile (warp-uniform)
+      const bool diag = n0 + BN > pos0 || n0 + BN > S_kv || (W > 0 && n0 < pos0 + BM - W);
       if (diag) {
+        const int lo = W > 0 ? qpos - W + 1 : INT_MIN;
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const int kp = n0 + c;
-          if (kp > qpos || kp >= S_kv) sv[c] = -INFINITY;
+          if (kp > qpos || kp >= S_kv || kp < lo) sv[c] = -INFINITY;
         }
       }
       // row max of the raw scores (the scale is positive, so it commutes)
@@ -698,6 +707,7 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   p.S = a.S;
   p.q_start = a.q_start;
   p.S_kv = S_kv;
+  p.window = a.window;
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
   const size_t smem = prefill_smem_bytes<D, NSRC, G>();
   auto kern = prefill_kernel<D, NSRC, G>;

@@ -68,6 +68,7 @@ _SIGS = {
     "fkv_set_fusion_weights": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P]),
     "fkv_set_sources": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int]),
+    "fkv_set_window": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int]),
     "fkv_append_kv": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, ctypes.c_int, _P]),
     "fkv_decode_workspace_bytes": (ctypes.c_size_t, [_P]),
     "fkv_decode_attn": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, _P, _P, _P,
@@ -209,6 +210,9 @@ class Context:
         m = MODES[mode] if isinstance(mode, str) else int(mode)
         _check(self._lib.fkv_set_sources(self.handle, layer, m, k_first, k_second, v_first,
                                          v_second), "fkv_set_sources")
+
+    def fkv_set_window(self, layer: int, window: int):
+        _check(self._lib.fkv_set_window(self.handle, layer, window), "fkv_set_window")
 
     def fkv_append_kv(self, layer: int, k_new, v_new, pos, T: Optional[int] = None, stream=None):
         c = self.cfg

@@ -123,6 +123,18 @@ fkv_status fkv_set_fusion_weights(fkv_ctx* ctx, int layer, const float* a_first,
 fkv_status fkv_set_sources(fkv_ctx* ctx, int layer, int mode, int k_first, int k_second,
                            int v_first, int v_second);
 
+/* Make `layer` a sliding-window layer: its decode and prefill calls attend
+ * only to the last `window` positions (keys t with m - window < t <= m for a
+ * query at position m); 0 restores full attention (the default).  This is the
+ * hybrid sliding-window setting of the FusedKV slides ("MoE and hybrid SWA":
+ * window 512, three window layers per full-attention layer).  With
+ * fkv_set_sources, window upper layers reconstruct from window storage layers
+ * and full layers from full ones (sources typed by attention kind).  The
+ * caches keep their [B, H_kv, S_max, D] layout; a window layer reads only
+ * rows [len - window, len).  FKV_ERR_INVALID_ARG for a bad layer or a
+ * negative window. */
+fkv_status fkv_set_window(fkv_ctx* ctx, int layer, int window);
+
 /* Write the post-RoPE K/V of T new tokens into a layer's cache (the storage
  * caches take the new token before the upper layers attend; reading notes
  * §2.3).  k_new, v_new: device [B, H_kv, T, D] in the context dtype.

@@ -54,7 +54,7 @@ class DecodeSetup:
     to a library context."""
 
     def __init__(self, w, layer, modes, seed=0, device="cuda", lens=None, decode_ctas=0,
-                 weight_std=0.3, tie_keys=True, sources=None):
+                 weight_std=0.3, tie_keys=True, sources=None, window=0):
         """``sources``: {mode: (k_first, k_second, v_first, v_second)} to
         reconstruct from other storage layers (all storage layers are bound)."""
         import cross_layer_kv_gb300 as fkv
@@ -80,6 +80,9 @@ class DecodeSetup:
             self.ctx.fkv_set_fusion_weights(layer, *self.weights)
         for m, src in self.sources.items():
             self.ctx.fkv_set_sources(layer, m, *src)
+        self.window = window
+        if window:
+            self.ctx.fkv_set_window(layer, window)
         self.q = synth.make_query(w, layer, seed, device)
         if lens is None:
             self.lens = synth.make_seq_lens(w, seed, device)
@@ -107,6 +110,7 @@ class DecodeSetup:
         lens = self.lens.cpu().tolist()
         G = w.group
         sk = self.source_kwargs(mode)
+        sk["window"] = self.window
         if pairs is None:
             kc = {l: f64(k) for l, (k, v) in self.caches.items()}
             vc = {l: f64(v) for l, (k, v) in self.caches.items()}

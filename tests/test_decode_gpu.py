@@ -232,3 +232,41 @@ def test_set_sources_rejects_non_storage_layers():
     with pytest.raises(B.FkvError):
         s.ctx.fkv_set_sources(2, "lite", 1, 0, 1, 0)   # a storage layer has no sources
     s.close()
+
+
+
+# ---------------------------------------------------------------------------
+# sliding-window layers (hybrid SWA, FusedKV slides "MoE and hybrid SWA")
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("window", [1, 37, 300, 2000])
+@pytest.mark.parametrize("mode", ALL_MODES)
+@pytest.mark.parametrize("D", [64, 80])
+def test_window_decode(window, mode, D):
+    w = _small(D, 2, S=700, Bt=3)
+    s = DecodeSetup(w, 5, [mode], seed=17, lens=[700, 1, 333], window=window)
+    assert_close(f64(s.run(mode)), s.oracle(mode), "bf16", "W=%d %s D=%d" % (window, mode, D))
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    s.close()
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_window_decode_full_size_332M(mode):
+    """332M workload with the pages' window of 512 (sampled rows)."""
+    w = synth.M332
+    s = DecodeSetup(w, w.num_layers, [mode], seed=0, window=512)
+    got = f64(s.run(mode))
+    pairs = _pairs(w, 6, 19)
+    assert_close(np.stack([got[b, h] for b, h in pairs]), s.oracle(mode, pairs), "bf16",
+                 "332M W=512 %s" % mode)
+    s.close()
+    torch.cuda.empty_cache()
+
+
+def test_set_window_rejects():
+    w = _small(64, 2, S=64, Bt=1)
+    s = DecodeSetup(w, 5, ["lite"], seed=18, lens=[64])
+    for layer, win in ((0, 4), (7, 4), (5, -1)):
+        with pytest.raises(B.FkvError):
+            s.ctx.fkv_set_window(layer, win)
+    s.close()

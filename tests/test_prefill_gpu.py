@@ -24,9 +24,10 @@ def _cuda():
 
 
 class PrefillSetup:
-    def __init__(self, w, layer, mode, S, seed=0, tie_keys=True, sources=None):
+    def __init__(self, w, layer, mode, S, seed=0, tie_keys=True, sources=None, window=0):
         self.w, self.layer, self.mode, self.S = w, layer, mode, S
         self.sources = sources
+        self.window = window
         n = w.n
         need = [layer] if (layer <= n or mode == "vanilla") else sorted({1, n})
         if sources:
@@ -44,6 +45,8 @@ class PrefillSetup:
             self.ctx.fkv_set_fusion_weights(layer, *self.weights)
         if sources:
             self.ctx.fkv_set_sources(layer, mode, *sources)
+        if window:
+            self.ctx.fkv_set_window(layer, window)
         g = torch.Generator(device="cuda").manual_seed(seed + 99)
         self.q = torch.randn(w.batch, w.q_heads, S, w.head_dim, generator=g,
                              device="cuda").to(torch.bfloat16)
@@ -65,6 +68,7 @@ class PrefillSetup:
         w = self.w
         G = w.group
         sk = self.source_kwargs()
+        sk["window"] = self.window
         ws = ({self.layer: tuple(f64(x) for x in self.weights)} if self.weights else None)
         if bh is None:
             kc = {l: f64(k) for l, (k, v) in self.caches.items()}
@@ -170,7 +174,7 @@ def _chunk_oracle(s, q, q_start, bh=None, rows=None):
         kc = {l: f64(k[:, :, :n]) for l, (k, v) in s.caches.items()}
         vc = {l: f64(v[:, :, :n]) for l, (k, v) in s.caches.items()}
         return O.chunk_prefill_attn(f64(q), q_start, s.layer, w.num_layers, s.mode, kc, vc,
-                                    weights=ws)
+                                    weights=ws, window=s.window)
     b, h = bh
     kh = h // w.group
     kc = {l: f64(k[b:b + 1, kh:kh + 1, :n]) for l, (k, v) in s.caches.items()}
@@ -181,10 +185,11 @@ def _chunk_oracle(s, q, q_start, bh=None, rows=None):
     if rows is not None:
         # rows of the chunk, each a one-row chunk at its own position
         return np.stack([O.chunk_prefill_attn(f64(qq[:, :, r:r + 1]), q_start + r, s.layer,
-                                              w.num_layers, s.mode, kc, vc, weights=ws)[0, 0, 0]
+                                              w.num_layers, s.mode, kc, vc, weights=ws,
+                                              window=s.window)[0, 0, 0]
                          for r in rows])
     return O.chunk_prefill_attn(f64(qq), q_start, s.layer, w.num_layers, s.mode, kc, vc,
-                                weights=ws)[0, 0]
+                                weights=ws, window=s.window)[0, 0]
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -259,4 +264,25 @@ def test_prefill_sources_and_scaled(mode, src, D):
     w = synth.Workload("p6", 6, 2, 260, 4, 2, D, "bf16")   # storage layers 1..3
     s = PrefillSetup(w, 5, mode, 250, seed=9, sources=src)
     assert_close(f64(s.run()), s.oracle(), "bf16", "prefill %s %s D=%d" % (mode, src, D))
+    s.close()
+
+
+
+@pytest.mark.parametrize("window", [1, 16, 64, 100, 300])
+@pytest.mark.parametrize("mode", ["vanilla", "fused", "scaled"])
+def test_prefill_window(window, mode):
+    w = _w(96, 2, 320)
+    s = PrefillSetup(w, 4, mode, 300, seed=10, window=window)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "prefill W=%d %s" % (window, mode))
+    s.close()
+
+
+def test_prefill_window_chunk():
+    w = _w(64, 2, 400)
+    s = PrefillSetup(w, 4, "fused", 400, seed=11, window=77)
+    for a, c in ((0, 130), (130, 200), (330, 70)):
+        qc = s.q[:, :, a:a + c].contiguous()
+        oc = torch.empty_like(qc)
+        s.ctx.fkv_prefill_attn_chunk(qc, 4, "fused", a, c, oc)
+        assert_close(f64(oc), _chunk_oracle(s, qc, a), "bf16", "window chunk %d+%d" % (a, c))
     s.close()
