@@ -297,6 +297,93 @@ def append_kv(cache: np.ndarray, new: np.ndarray, pos: Sequence[int]) -> np.ndar
 
 
 # ---------------------------------------------------------------------------
+# 4-bit KV cache ([Slides] "Four-bit KV quantization is the stronger
+# combination", Table 14).  KIVI's grouping is not on the pages; this build
+# quantises each token row of each head in groups of Q4_GROUP channels with
+# an asymmetric uniform 4-bit code:
+#     min = min(x_g), scale = bf16((max(x_g) - min) / 15)   (fp32 division),
+#     code = clamp(rint((x - min) / scale), 0, 15)           (fp32, half to even),
+#     x_hat = min + code * scale.
+# A constant group (scale 0) stores code 0.  min and scale are stored as bf16
+# (min is an input value, so exact); the codes use the stored scale.
+# ---------------------------------------------------------------------------
+
+Q4_GROUP = 16
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """float32 -> nearest bfloat16 (ties to even), returned as float32."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32)
+
+
+def q4_quantize(x: np.ndarray):
+    """x ``[..., D]`` (bf16 values) -> codes uint8 ``[..., D]`` (0..15),
+    scale and min float32 ``[..., D / Q4_GROUP]`` (bf16-representable)."""
+    x = np.asarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    g = x.reshape(x.shape[:-1] + (D // Q4_GROUP, Q4_GROUP))
+    lo = g.min(axis=-1)
+    hi = g.max(axis=-1)
+    scale = bf16_round((hi - lo) / np.float32(15.0))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint((g - lo[..., None]) / scale[..., None])
+    q = np.where(scale[..., None] > 0, q, 0)
+    codes = np.clip(q, 0, 15).astype(np.uint8).reshape(x.shape)
+    return codes, scale.astype(np.float32), lo.astype(np.float32)
+
+
+def q4_dequantize(codes: np.ndarray, scale: np.ndarray, lo: np.ndarray) -> np.ndarray:
+    """x_hat = min + code * scale, float64 ``[..., D]``."""
+    D = codes.shape[-1]
+    c = np.asarray(codes, dtype=np.float64).reshape(codes.shape[:-1] + (D // Q4_GROUP, Q4_GROUP))
+    xh = np.asarray(lo, np.float64)[..., None] + c * np.asarray(scale, np.float64)[..., None]
+    return xh.reshape(codes.shape)
+
+
+def q4_row_bytes(head_dim: int) -> int:
+    """Bytes of one quantised row: codes (D/2), then (scale, min) bf16 pairs
+    (D/4), padded to 16 bytes."""
+    return (head_dim // 2 + head_dim // 4 + 15) // 16 * 16
+
+
+def q4_pack(codes: np.ndarray, scale: np.ndarray, lo: np.ndarray) -> np.ndarray:
+    """Rows ``[..., D]`` -> records ``[..., q4_row_bytes(D)]`` uint8: byte i of
+    the codes holds channel 2i in its low and 2i+1 in its high nibble; then
+    per group the bf16 bits of scale and of min (little-endian)."""
+    D = codes.shape[-1]
+    rb = q4_row_bytes(D)
+    out = np.zeros(codes.shape[:-1] + (rb,), dtype=np.uint8)
+    c = codes.astype(np.uint8)
+    out[..., : D // 2] = c[..., 0::2] | (c[..., 1::2] << 4)
+    sb = (np.ascontiguousarray(scale, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    mb = (np.ascontiguousarray(lo, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    pm = np.stack([sb, mb], axis=-1).reshape(codes.shape[:-1] + (D // Q4_GROUP * 2,))
+    out[..., D // 2: D // 2 + D // 4] = pm.view(np.uint8).reshape(codes.shape[:-1] + (D // 4,))
+    return out
+
+
+def q4_unpack(rec: np.ndarray, head_dim: int):
+    """Records -> (codes, scale, min), the inverse of ``q4_pack``."""
+    D = head_dim
+    rec = np.asarray(rec, dtype=np.uint8)
+    b = rec[..., : D // 2]
+    codes = np.empty(rec.shape[:-1] + (D,), dtype=np.uint8)
+    codes[..., 0::2] = b & 0xF
+    codes[..., 1::2] = b >> 4
+    pm = np.ascontiguousarray(rec[..., D // 2: D // 2 + D // 4]).view(np.uint16)
+    pm = pm.reshape(rec.shape[:-1] + (D // Q4_GROUP, 2)).astype(np.uint32) << 16
+    f = pm.view(np.float32)
+    return codes, f[..., 0].copy(), f[..., 1].copy()
+
+
+def q4_dequantize_records(rec: np.ndarray, head_dim: int) -> np.ndarray:
+    return q4_dequantize(*q4_unpack(rec, head_dim))
+
+
+# ---------------------------------------------------------------------------
 # RoPE and the pair-tying property ([Slides] "Post-RoPE fusion needs paired key
 # weights", Eqs.(7)-(8); [Notes] §2.4)
 # ---------------------------------------------------------------------------

@@ -565,3 +565,67 @@ def test_window_prefill_matches_sdpa_band_mask():
     # chunked, windowed: rows of the full windowed prefill
     part = O.chunk_prefill_attention(q[:, :, 11:20], 11, k, v, window=W)
     np.testing.assert_allclose(part, got[:, :, 11:20], atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# 4-bit KV cache ([Slides] Table 14); the grouping is this build's reading
+# --------------------------------------------------------------------------
+
+def test_bf16_round_matches_torch():
+    rng = _rng(27)
+    x = (rng.standard_normal(10000) * 10 ** rng.uniform(-5, 5, 10000)).astype(np.float32)
+    x[:4] = [1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 0.0]   # exact ties
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    np.testing.assert_array_equal(O.bf16_round(x), ref)
+
+
+def test_q4_error_bound_codes_and_grid():
+    rng = _rng(28)
+    x = O.bf16_round(rng.standard_normal((7, 3, 64)).astype(np.float32))
+    codes, scale, lo = O.q4_quantize(x)
+    assert codes.dtype == np.uint8 and codes.max() <= 15
+    xh = O.q4_dequantize(codes, scale, lo)
+    # |x - x_hat| <= scale / 2 (+ the scale's own bf16 rounding over 15 steps)
+    s = np.repeat(scale, O.Q4_GROUP, axis=-1).astype(np.float64)
+    hi = np.repeat(x.reshape(7, 3, 4, 16).max(-1), 16, axis=-1)
+    bound = 0.5 * s + np.abs(hi - (np.repeat(lo, 16, -1) + 15 * s)) + 1e-12
+    assert np.all(np.abs(x - xh) <= bound)
+    # values already on the grid round-trip exactly
+    again = O.q4_quantize(O.bf16_round(xh.astype(np.float32)))
+    np.testing.assert_array_equal(O.q4_dequantize(*again), O.q4_dequantize(codes, scale, lo))
+    # a constant group stores code 0 and dequantises exactly
+    cst = np.full((1, 16), 1.5, np.float32)
+    c2, s2, l2 = O.q4_quantize(cst)
+    assert np.all(c2 == 0) and s2[0, 0] == 0 and np.all(O.q4_dequantize(c2, s2, l2) == 1.5)
+
+
+def test_q4_pack_roundtrip_and_layout():
+    rng = _rng(29)
+    for D in (64, 80, 96, 128):
+        x = O.bf16_round(rng.standard_normal((2, 5, D)).astype(np.float32))
+        codes, scale, lo = O.q4_quantize(x)
+        rec = O.q4_pack(codes, scale, lo)
+        assert rec.shape[-1] == O.q4_row_bytes(D) and rec.shape[-1] % 16 == 0
+        c2, s2, l2 = O.q4_unpack(rec, D)
+        np.testing.assert_array_equal(c2, codes)
+        np.testing.assert_array_equal(s2, scale)
+        np.testing.assert_array_equal(l2, lo)
+        # byte 0 holds channel 0 (low nibble) and channel 1 (high nibble)
+        assert rec[0, 0, 0] == codes[0, 0, 0] | (codes[0, 0, 1] << 4)
+    assert [O.q4_row_bytes(d) for d in (64, 80, 96, 128)] == [48, 64, 80, 96]
+
+
+def test_q4_attention_is_attention_over_dequantised_caches():
+    rng = _rng(30)
+    L, B, H_kv, S, D = 4, 1, 2, 20, 32
+    kc, vc = _caches(rng, L, B, H_kv, S, D, layers=[1, 2])
+    kq = {l: O.q4_dequantize_records(O.q4_pack(*O.q4_quantize(O.bf16_round(k.astype(np.float32)))), D)
+          for l, k in kc.items()}
+    vq = {l: O.q4_dequantize_records(O.q4_pack(*O.q4_quantize(O.bf16_round(v.astype(np.float32)))), D)
+          for l, v in vc.items()}
+    q = rng.standard_normal((B, 4, D))
+    ws = {3: _weights(rng, H_kv, D)}
+    got = O.decode_attn(q, 3, L, O.FUSED, kq, vq, [S], weights=ws)
+    full = O.decode_attn(q, 3, L, O.FUSED, kc, vc, [S], weights=ws)
+    # 4-bit noise, not a different function: close to the unquantised result
+    assert np.max(np.abs(got - full)) < 0.2
