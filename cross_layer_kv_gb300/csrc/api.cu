@@ -25,6 +25,7 @@ struct fkv_ctx {
   std::vector<int> lite_src[2];            // lite / scaled sources: K, V
   std::vector<int> fused_src[4];           // fused sources: K first, K second, V first, V second
   std::vector<int> window;                 // sliding window per layer (0: full attention)
+  std::vector<char> q4;                    // layer cache holds 4-bit records
 };
 
 namespace {
@@ -56,18 +57,21 @@ fkv_status check_config(const fkv_config* c) {
 }
 
 // Resolve the cache / weight sources of a call.  nsrc = 1 or 2.
-fkv_status resolve_sources(const fkv_ctx* c, int layer, int mode, const void* k[2],
-                           const void* v[2], const float* a[2], const float* b[2], int* nsrc) {
+fkv_status resolve_sources_impl(const fkv_ctx* c, int layer, int mode, const void* k[2],
+                                const void* v[2], const float* a[2], const float* b[2], int* nsrc,
+                                int src[4]) {
   if (layer < 1 || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
   if (mode != FKV_VANILLA && mode != FKV_LITE && mode != FKV_FUSED && mode != FKV_SCALED)
     return FKV_ERR_INVALID_ARG;
   k[0] = k[1] = v[0] = v[1] = nullptr;
   a[0] = a[1] = b[0] = b[1] = nullptr;
   const int n = c->n;
+  src[0] = src[1] = src[2] = src[3] = 0;
   if (layer <= n || mode == FKV_VANILLA) {
     if (layer > n && !c->cfg.store_upper) return FKV_ERR_UNSUPPORTED;
     k[0] = c->k[layer];
     v[0] = c->v[layer];
+    src[0] = src[2] = layer;
     *nsrc = 1;
     if (!k[0] || !v[0]) return FKV_ERR_INVALID_ARG;
     return FKV_OK;
@@ -75,6 +79,8 @@ fkv_status resolve_sources(const fkv_ctx* c, int layer, int mode, const void* k[
   if (mode == FKV_LITE || mode == FKV_SCALED) {  // K^i = K^s, V^i = V^t (default n, 1)
     k[0] = c->k[c->lite_src[0][layer]];
     v[0] = c->v[c->lite_src[1][layer]];
+    src[0] = c->lite_src[0][layer];
+    src[2] = c->lite_src[1][layer];
     *nsrc = 1;
     if (!k[0] || !v[0]) return FKV_ERR_INVALID_ARG;
     if (mode == FKV_SCALED) {  // a_first scales K, b_first scales V
@@ -89,6 +95,7 @@ fkv_status resolve_sources(const fkv_ctx* c, int layer, int mode, const void* k[
   k[1] = c->k[c->fused_src[1][layer]];
   v[0] = c->v[c->fused_src[2][layer]];
   v[1] = c->v[c->fused_src[3][layer]];
+  for (int i = 0; i < 4; ++i) src[i] = c->fused_src[i][layer];
   for (int i = 0; i < 2; ++i) {
     a[i] = c->w[i][layer];
     b[i] = c->w[2 + i][layer];
@@ -96,6 +103,25 @@ fkv_status resolve_sources(const fkv_ctx* c, int layer, int mode, const void* k[
   *nsrc = 2;
   if (!k[0] || !k[1] || !v[0] || !v[1] || !a[0] || !a[1] || !b[0] || !b[1])
     return FKV_ERR_INVALID_ARG;
+  return FKV_OK;
+}
+
+// Sources and their storage format: *q4 = 1 if every source layer holds
+// 4-bit records, 0 if none does; a mix is FKV_ERR_UNSUPPORTED.
+fkv_status resolve_sources(const fkv_ctx* c, int layer, int mode, const void* k[2],
+                           const void* v[2], const float* a[2], const float* b[2], int* nsrc,
+                           int* q4 = nullptr) {
+  int src[4];
+  const fkv_status s = resolve_sources_impl(c, layer, mode, k, v, a, b, nsrc, src);
+  if (s != FKV_OK) return s;
+  int nq = 0, nt = 0;
+  for (int i = 0; i < 4; ++i) {
+    if (src[i] <= 0) continue;
+    ++nt;
+    nq += c->q4[src[i]] ? 1 : 0;
+  }
+  if (nq != 0 && nq != nt) return FKV_ERR_UNSUPPORTED;
+  if (q4) *q4 = nq ? 1 : 0;
   return FKV_OK;
 }
 
@@ -132,6 +158,7 @@ fkv_status fkv_create(const fkv_config* cfg, fkv_ctx** out) {
   c->v.assign(cfg->num_layers + 1, nullptr);
   for (auto& w : c->w) w.assign(cfg->num_layers + 1, nullptr);
   c->window.assign(cfg->num_layers + 1, 0);
+  c->q4.assign(cfg->num_layers + 1, 0);
   c->lite_src[0].assign(cfg->num_layers + 1, c->n);  // K^n
   c->lite_src[1].assign(cfg->num_layers + 1, 1);     // V^1
   c->fused_src[0].assign(cfg->num_layers + 1, 1);
@@ -164,6 +191,23 @@ fkv_status fkv_bind_layer_cache(fkv_ctx* c, int layer, void* k, void* v) {
   if (!k || !v || !aligned16(k) || !aligned16(v)) return FKV_ERR_INVALID_ARG;
   c->k[layer] = k;
   c->v[layer] = v;
+  c->q4[layer] = 0;
+  return FKV_OK;
+}
+
+size_t fkv_q4_row_bytes(int head_dim) {
+  if (head_dim != 64 && head_dim != 80 && head_dim != 96 && head_dim != 128) return 0;
+  return (size_t)fkv::q4_row_bytes(head_dim);
+}
+
+fkv_status fkv_bind_layer_cache_q4(fkv_ctx* c, int layer, void* k_rec, void* v_rec) {
+  if (!c || layer < 1 || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
+  if (c->cfg.dtype != FKV_BF16 || c->group > 2) return FKV_ERR_UNSUPPORTED;
+  if (layer > c->n && !c->cfg.store_upper) return FKV_ERR_UNSUPPORTED;
+  if (!k_rec || !v_rec || !aligned16(k_rec) || !aligned16(v_rec)) return FKV_ERR_INVALID_ARG;
+  c->k[layer] = k_rec;
+  c->v[layer] = v_rec;
+  c->q4[layer] = 1;
   return FKV_OK;
 }
 
@@ -229,8 +273,9 @@ fkv_status fkv_append_kv(fkv_ctx* c, int layer, const void* k_new, const void* v
   a.head_dim = c->cfg.head_dim;
   a.T = T;
   a.elem_bytes = elem_bytes(c->cfg);
-  return fkv::append_launch(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FKV_OK
-                                                                                 : FKV_ERR_CUDA;
+  const cudaError_t e = c->q4[layer] ? fkv::append_q4_launch(a, static_cast<cudaStream_t>(stream))
+                                     : fkv::append_launch(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }
 
 size_t fkv_decode_workspace_bytes(const fkv_ctx* c) {
@@ -242,6 +287,8 @@ size_t fkv_decode_workspace_bytes(const fkv_ctx* c) {
     fkv::DecodePlan p{};
     if (fkv::decode_plan(d, c->num_sms, &p) == cudaSuccess && p.workspace_bytes > best)
       best = p.workspace_bytes;
+    if (fkv::decode_q4_plan(d, c->num_sms, &p) == cudaSuccess && p.workspace_bytes > best)
+      best = p.workspace_bytes;
   }
   return best;
 }
@@ -251,13 +298,16 @@ fkv_status fkv_decode_attn(fkv_ctx* c, const void* q, int layer, int mode,
                            size_t workspace_bytes, void* stream) {
   if (!c) return FKV_ERR_INVALID_ARG;
   fkv::DecodeArgs d = decode_args(c);
-  fkv_status s = resolve_sources(c, layer, mode, d.k, d.v, d.a, d.b, &d.nsrc);
+  int q4 = 0;
+  fkv_status s = resolve_sources(c, layer, mode, d.k, d.v, d.a, d.b, &d.nsrc, &q4);
   if (s != FKV_OK) return s;
   if (!q || !out || !seq_lens || !aligned16(q) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return FKV_ERR_INVALID_ARG;
   fkv::DecodePlan plan{};
-  if (fkv::decode_plan(d, c->num_sms, &plan) != cudaSuccess) return FKV_ERR_UNSUPPORTED;
+  const cudaError_t pe = q4 ? fkv::decode_q4_plan(d, c->num_sms, &plan)
+                            : fkv::decode_plan(d, c->num_sms, &plan);
+  if (pe != cudaSuccess) return FKV_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace) || workspace_bytes < plan.workspace_bytes)
     return FKV_ERR_WORKSPACE;
   d.q = q;
@@ -268,9 +318,9 @@ fkv_status fkv_decode_attn(fkv_ctx* c, const void* q, int layer, int mode,
   unsigned ep = g_decode_epoch.fetch_add(1);
   if (ep == 0) ep = g_decode_epoch.fetch_add(1);
   d.epoch = ep;
-  return fkv::decode_launch(d, plan, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? FKV_OK
-             : FKV_ERR_CUDA;
+  const cudaError_t e = q4 ? fkv::decode_q4_launch(d, plan, static_cast<cudaStream_t>(stream))
+                           : fkv::decode_launch(d, plan, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }
 
 fkv_status fkv_prefill_attn(fkv_ctx* c, const void* q, int layer, int mode, int S, void* out,
@@ -283,8 +333,10 @@ fkv_status fkv_prefill_attn_chunk(fkv_ctx* c, const void* q, int layer, int mode
   if (!c) return FKV_ERR_INVALID_ARG;
   const int S = C;
   fkv::PrefillArgs p{};
-  fkv_status s = resolve_sources(c, layer, mode, p.k, p.v, p.a, p.b, &p.nsrc);
+  int q4 = 0;
+  fkv_status s = resolve_sources(c, layer, mode, p.k, p.v, p.a, p.b, &p.nsrc, &q4);
   if (s != FKV_OK) return s;
+  if (q4) return FKV_ERR_UNSUPPORTED;   // prefill reads bf16 caches
   if (c->cfg.dtype != FKV_BF16) return FKV_ERR_UNSUPPORTED;
   if (S < 1 || q_start < 0 || (long long)q_start + S > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return FKV_ERR_INVALID_ARG;

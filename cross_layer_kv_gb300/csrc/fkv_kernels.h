@@ -77,6 +77,16 @@ struct AppendArgs {
 
 cudaError_t append_launch(const AppendArgs& a, cudaStream_t stream);
 
+// 4-bit caches: rows of q4_row_bytes(D) bytes (codes, then bf16 (scale, min)
+// per group of kQ4Group channels, padded to 16 bytes).
+constexpr int kQ4Group = 16;
+__host__ __device__ constexpr int q4_row_bytes(int head_dim) {
+  return (head_dim / 2 + head_dim / 4 + 15) / 16 * 16;
+}
+cudaError_t append_q4_launch(const AppendArgs& a, cudaStream_t stream);
+cudaError_t decode_q4_launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+cudaError_t decode_q4_plan(const DecodeArgs& a, int num_sms, DecodePlan* plan);
+
 constexpr int kDevTimeoutBit = 2;  // must match kDevTimeout
 
 struct PrefillArgs {

@@ -65,6 +65,8 @@ _SIGS = {
     "fkv_create": (ctypes.c_int, [ctypes.POINTER(fkv_config), ctypes.POINTER(_P)]),
     "fkv_destroy": (None, [_P]),
     "fkv_bind_layer_cache": (ctypes.c_int, [_P, ctypes.c_int, _P, _P]),
+    "fkv_q4_row_bytes": (ctypes.c_size_t, [ctypes.c_int]),
+    "fkv_bind_layer_cache_q4": (ctypes.c_int, [_P, ctypes.c_int, _P, _P]),
     "fkv_set_fusion_weights": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P]),
     "fkv_set_sources": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int]),
@@ -194,6 +196,24 @@ class Context:
         _check(self._lib.fkv_bind_layer_cache(self.handle, layer, _ptr(k), _ptr(v)),
                "fkv_bind_layer_cache")
         self._keep[("kv", layer)] = (k, v)
+
+    def fkv_q4_row_bytes(self) -> int:
+        return int(self._lib.fkv_q4_row_bytes(self.cfg.head_dim))
+
+    def q4_cache(self, device="cuda") -> torch.Tensor:
+        """A zeroed uint8 [B, H_kv, S_max, fkv_q4_row_bytes(D)] buffer."""
+        c = self.cfg
+        return torch.zeros((c.batch, c.num_kv_heads, c.max_seq, self.fkv_q4_row_bytes()),
+                           dtype=torch.uint8, device=device)
+
+    def fkv_bind_layer_cache_q4(self, layer: int, k_rec, v_rec):
+        c = self.cfg
+        shape = (c.batch, c.num_kv_heads, c.max_seq, self.fkv_q4_row_bytes())
+        self._need(k_rec, shape, torch.uint8, "k records")
+        self._need(v_rec, shape, torch.uint8, "v records")
+        _check(self._lib.fkv_bind_layer_cache_q4(self.handle, layer, _ptr(k_rec), _ptr(v_rec)),
+               "fkv_bind_layer_cache_q4")
+        self._keep[("kv", layer)] = (k_rec, v_rec)
 
     def fkv_set_fusion_weights(self, layer: int, a_first, a_second, b_first, b_second):
         shape = (self.cfg.num_kv_heads, self.cfg.head_dim)

@@ -104,6 +104,25 @@ void fkv_destroy(fkv_ctx* ctx);
  * outlive their use. */
 fkv_status fkv_bind_layer_cache(fkv_ctx* ctx, int layer, void* k, void* v);
 
+/* Bytes of one row of a 4-bit cache for head dim D (0 if D is unsupported):
+ * D/2 bytes of codes, D/4 bytes of parameters, padded to 16 bytes
+ * (48, 64, 80, 96 for D = 64, 80, 96, 128). */
+size_t fkv_q4_row_bytes(int head_dim);
+
+/* Register 4-bit K and V caches of a layer (FusedKV slides, "Four-bit KV
+ * quantization is the stronger combination", Table 14; the quantisation
+ * grouping is this library's, the pages do not give KIVI's):
+ * k_rec, v_rec: device, [B, H_kv, S_max, fkv_q4_row_bytes(D)] bytes,
+ * 16-byte aligned.  Each row holds its D channels in groups of 16 as 4-bit
+ * codes (byte i: channel 2i in the low nibble, 2i+1 in the high one),
+ * followed by one (scale, min) bf16 pair per group: x = min + code * scale.
+ * fkv_append_kv quantises new rows of such a layer (min/max of the group,
+ * scale = bf16((max - min) / 15), code = clamp(rint((x - min) / scale),
+ * 0, 15)); fkv_decode_attn reads, dequantises and fuses them in registers when
+ * every source layer of the call is 4-bit (a mix of formats, and prefill, give
+ * FKV_ERR_UNSUPPORTED).  Needs dtype FKV_BF16 and H_q / H_kv <= 2. */
+fkv_status fkv_bind_layer_cache_q4(fkv_ctx* ctx, int layer, void* k_rec, void* v_rec);
+
 /* Register the fusion weights of reconstruction layer n < layer <= L
  * (FusedKV slides, Eqs.(4)-(5)): a_first/a_second scale K^1/K^n, b_first/
  * b_second scale V^1/V^n.  Each is a device fp32 [H_kv, D] buffer owned by the
