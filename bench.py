@@ -344,8 +344,9 @@ def main():
     ap.add_argument("--no-other-decode", action="store_true",
                     help="skip the single-call timings of the 1.5B and 4B decode workloads")
     ap.add_argument("--profile", default=None,
-                    help="run one call type only, e.g. decode:fused:332M-decode or "
-                         "prefill:fused:650M-prefill (for ncu captures)")
+                    help="run one call type only, e.g. decode:fused:332M-decode, "
+                         "decode:fused:332M-decode:q4 or prefill:fused:650M-prefill "
+                         "(for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -435,8 +436,10 @@ def main():
     if not args.no_prefill:
         prefill = bench_prefill(device, stream, peaks, W)
     other_decode = None
+    q4 = None
     if not args.no_other_decode:
         other_decode = bench_decode_calls(device, stream, peaks, W)
+        q4 = bench_q4_calls(device, stream, peaks, W)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -475,15 +478,18 @@ def main():
             line["prefill"] = prefill
         if other_decode is not None:
             line["decode_other_workloads"] = other_decode
+        if q4 is not None:
+            line["decode_q4_332M"] = q4
         print(json.dumps(line), flush=True)
     if dist_on:
         torch.distributed.destroy_process_group()
 
 
 class SingleCall:
-    """Buffers for one call type of a workload: only the layers it reads."""
+    """Buffers for one call type of a workload: only the layers it reads
+    (4-bit caches with ``q4``, quantised by the library's own append)."""
 
-    def __init__(self, kind, mode, w, device, stream):
+    def __init__(self, kind, mode, w, device, stream, q4=False):
         import cross_layer_kv_gb300 as fkv
         from cross_layer_kv_gb300 import synth
         self.w, self.kind, self.mode = w, kind, mode
@@ -494,8 +500,17 @@ class SingleCall:
         self.keep = []
         for l in need:
             k, v = synth.make_cache(w, l, 0, device)
-            self.keep.append((k, v))
-            self.ctx.fkv_bind_layer_cache(l, k, v)
+            if q4:
+                kr, vr = self.ctx.q4_cache(device), self.ctx.q4_cache(device)
+                self.ctx.fkv_bind_layer_cache_q4(l, kr, vr)
+                pos0 = torch.zeros(w.batch, dtype=torch.int32, device=device)
+                self.ctx.fkv_append_kv(l, k, v, pos0, w.seq, stream)
+                torch.cuda.synchronize()
+                self.keep.append((kr, vr))
+                del k, v
+            else:
+                self.keep.append((k, v))
+                self.ctx.fkv_bind_layer_cache(l, k, v)
         wts = synth.make_weights(w, layer, 0, device)
         self.keep.append(wts)
         self.ctx.fkv_set_fusion_weights(layer, *wts)
@@ -508,7 +523,8 @@ class SingleCall:
             self.keep += [q, out, lens, ws]
             self.call = lambda: ctx.fkv_decode_attn(q, layer, mode, lens, out, ws, stream)
             nsrc = 2 if mode == "fused" else 1
-            self.bytes = 2 * nsrc * w.kv_heads * int(lens.sum()) * w.head_dim * w.elem_bytes
+            row = ctx.fkv_q4_row_bytes() if q4 else w.head_dim * w.elem_bytes
+            self.bytes = 2 * nsrc * w.kv_heads * int(lens.sum()) * row
             self.flops = 0
         else:
             q = synth.make_query(w, layer, 0, device, positions=w.seq)
@@ -540,9 +556,11 @@ def run_profile_case(args, device):
     """One call type on its own, W warm-up calls then K timed calls; prints
     the mean call time.  Used for ncu captures of a single kernel."""
     from cross_layer_kv_gb300 import synth
-    kind, mode, wname = args.profile.split(":")
+    parts = args.profile.split(":")
+    kind, mode, wname = parts[:3]
+    q4 = len(parts) > 3 and parts[3] == "q4"
     stream = torch.cuda.Stream(device)
-    sc = SingleCall(kind, mode, synth.WORKLOADS[wname], device, stream)
+    sc = SingleCall(kind, mode, synth.WORKLOADS[wname], device, stream, q4=q4)
     us = sc.time_us(stream, args.steps, args.warmup)
     res = {"profile": args.profile, "call_us": us}
     if sc.bytes:
@@ -552,6 +570,24 @@ def run_profile_case(args, device):
         res["TFLOPs"] = sc.flops / (us * 1e-6) / 1e12
     print(json.dumps(res), flush=True)
     sc.close()
+
+
+def bench_q4_calls(device, stream, peaks, W, reps=20):
+    """4-bit caches: one upper-layer decode call per mode of the 332M-shaped
+    workload; GB/s over the 4-bit bytes, and the time against bf16."""
+    from cross_layer_kv_gb300 import synth
+    w = synth.M332
+    res = {"workload": w.name + " with 4-bit caches (16-channel groups, bf16 scale/min)"}
+    for mode in ("vanilla", "lite", "fused"):
+        sc = SingleCall("decode", mode, w, device, stream, q4=True)
+        us = sc.time_us(stream, reps, W)
+        gbs = sc.bytes / (us * 1e-6) / 1e9
+        res[mode] = {"upper_call_us": us, "bytes": sc.bytes, "GBps": gbs,
+                     "pct_of_measured_hbm": 100.0 * gbs / peaks["hbm_gbs"]}
+        sc.close()
+        del sc
+        torch.cuda.empty_cache()
+    return res
 
 
 def bench_decode_calls(device, stream, peaks, W, reps=20):

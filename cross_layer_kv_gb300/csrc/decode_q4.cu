@@ -10,9 +10,10 @@
 // channels of a row (8 bytes of codes, 4 bytes of parameters), so a row takes
 // C = D/16 lanes and a warp step covers R = 32/C rows.  The dequantisation is
 // folded into the dot products:
-//   q . (m + c * s)            = m * sum(q) + s * (q . c)       per group,
-//   sum_t p_t (m_t + c_t s_t)  = sum_t p_t m_t + sum_t (p_t s_t) c_t,
-// so each element costs a nibble-to-float conversion and one (packed) FMA;
+//   q . (m + c * s)            = m' * sum(q) + s * (q . (128 + c)),
+//   sum_t p_t (m_t + c_t s_t)  = sum_t p_t m'_t + sum_t (p_t s_t) (128 + c_t),
+// with m' = m - 128 s per group and row, so each element costs one byte
+// permute (128 + c is built exactly in the mantissa) and one packed FMA;
 // sum(q) per group is computed once per (b, kv-head) unit.
 #include "decode_impl.cuh"
 
@@ -37,17 +38,20 @@ struct Q4Cfg {
 };
 
 // 16 four-bit codes (two 32-bit words, channel 2i in the low nibble of byte
-// i) -> fp32 values 0..15.  Each byte is moved under the exponent of 2^23
-// (one byte permute) and the bias subtracted exactly.
-__device__ __forceinline__ void codes16(uint32_t w0, uint32_t w1, float* c) {
+// i) -> fp32 values 128 + code, exactly: one byte permute per code places it
+// in the mantissa under the exponent of 128 (0x43000000 | code << 16).  The
+// bias of 128 is folded into the group minimum by the caller (m - 128 s), so
+// no per-element subtraction is needed; products q * (128 + c) keep full
+// fp32 accuracy.
+__device__ __forceinline__ void codes16_biased(uint32_t w0, uint32_t w1, float* c) {
   const uint32_t ws[2] = {w0, w1};
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const uint32_t lo = ws[k] & 0x0F0F0F0Fu, hi = (ws[k] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      c[8 * k + 2 * b] = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540 | b)) - 8388608.f;
-      c[8 * k + 2 * b + 1] = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540 | b)) - 8388608.f;
+      c[8 * k + 2 * b] = __uint_as_float(__byte_perm(lo, 0x43000000u, 0x7054 | (b << 8)));
+      c[8 * k + 2 * b + 1] = __uint_as_float(__byte_perm(hi, 0x43000000u, 0x7054 | (b << 8)));
     }
   }
 }
@@ -254,15 +258,16 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
           const uint2 cw = *reinterpret_cast<const uint2*>(rp + c * 8);
           float sc, mn;
           q4_params(*reinterpret_cast<const uint32_t*>(rp + D / 2 + c * 4), sc, mn);
+          const float mb = fmaf(-128.f, sc, mn);   // x = (m - 128 s) + (128 + c) s
           float cf[E];
-          codes16(cw.x, cw.y, cf);
+          codes16_biased(cw.x, cw.y, cf);
 #pragma unroll
           for (int hq = 0; hq < G; ++hq) {
             float d0 = 0.f, d1 = 0.f;
 #pragma unroll
             for (int e = 0; e < E; e += 2)
               fma2(d0, d1, qa[sidx][hq][e], qa[sidx][hq][e + 1], cf[e], cf[e + 1]);
-            acc[hq] += mn * qsum[sidx][hq] + sc * (d0 + d1);
+            acc[hq] += mb * qsum[sidx][hq] + sc * (d0 + d1);
           }
         }
       }
@@ -310,12 +315,13 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
           const uint2 cw = *reinterpret_cast<const uint2*>(rp + c * 8);
           float sc, mn;
           q4_params(*reinterpret_cast<const uint32_t*>(rp + D / 2 + c * 4), sc, mn);
+          const float mb = fmaf(-128.f, sc, mn);
           float cf[E];
-          codes16(cw.x, cw.y, cf);
+          codes16_biased(cw.x, cw.y, cf);
 #pragma unroll
           for (int hq = 0; hq < G; ++hq) {
             const float ps = pj[hq] * sc;
-            om[sidx][hq] = fmaf(pj[hq], mn, om[sidx][hq]);
+            om[sidx][hq] = fmaf(pj[hq], mb, om[sidx][hq]);
 #pragma unroll
             for (int e = 0; e < E; e += 2)
               fma2(oc[sidx][hq][e], oc[sidx][hq][e + 1], ps, ps, cf[e], cf[e + 1]);
