@@ -104,8 +104,10 @@ struct PrefillArgs {
   float softmax_scale;
 };
 
-// Returns cudaErrorNotSupported for shapes the tensor-core kernel does not
-// cover.
+// Returns cudaErrorNotSupported for shapes the tensor-core kernels do not
+// cover.  One source (nsrc = 1) runs the 128-key kernel of prefill_wide.cu;
+// two sources (fused) the 64-key kernel with in-place fusion of prefill.cu.
 cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t prefill_wide_launch(const PrefillArgs& a, cudaStream_t stream);
 
 }  // namespace fkv

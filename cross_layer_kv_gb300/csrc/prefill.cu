@@ -31,187 +31,29 @@
 //  * Every wait is bounded; a wait that runs out sets an abort flag that
 //    every role checks, flags the device status, and the CTA releases its
 //    tensor memory and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <cfloat>
 #include <climits>
 #include <cstdint>
 #include <cstring>
-#include <mutex>
 
-#include "fkv_device.cuh"
 #include "fkv_kernels.h"
+#include "tc_device.cuh"
 
 namespace fkv {
 namespace {
 
 constexpr int BM = 128;       // query rows per CTA
 constexpr int BN = 64;        // keys per tile
-constexpr int SW = 64;        // swizzle span in bytes (32 bf16)
-constexpr int SWE = SW / 2;   // elements per swizzle row
+constexpr int SW = kSW;       // swizzle span in bytes (32 bf16)
+constexpr int SWE = kSWE;     // elements per swizzle row
 constexpr int TMEM_COLS = 512;
 constexpr int HEAD_COLS = 256;  // TMEM columns per head: S (BN) then O (D)
-
-// --- tcgen05 / TMA wrappers --------------------------------------------------
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(slot)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15]))
-      : "memory");
-}
-
-// 32 consecutive 32-bit TMEM columns of this thread's lane <- v.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-// D (TMEM) (+)= A (TMEM, 128 lanes x K packed bf16) * B (shared memory).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// (c0, c1) += (a0, a1) * (b0, b1): one packed fp32 FMA.
-__device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 A, B, C;\n\t"
-      "mov.b64 A, {%2, %3};\n\t"
-      "mov.b64 B, {%4, %5};\n\t"
-      "mov.b64 C, {%0, %1};\n\t"
-      "fma.rn.f32x2 C, A, B, C;\n\t"
-      "mov.b64 {%0, %1}, C;\n\t}"
-      : "+f"(c0), "+f"(c1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
-// (c0, c1) += (a0, a1): one packed fp32 add.
-__device__ __forceinline__ void add2(float& c0, float& c1, float a0, float a1) {
-  asm("{\n\t.reg .b64 A, C;\n\t"
-      "mov.b64 A, {%2, %3};\n\t"
-      "mov.b64 C, {%0, %1};\n\t"
-      "add.rn.f32x2 C, C, A;\n\t"
-      "mov.b64 {%0, %1}, C;\n\t}"
-      : "+f"(c0), "+f"(c1)
-      : "f"(a0), "f"(a1));
-}
-
-// Shared-memory matrix descriptor of tcgen05 (start, leading and stride byte
-// offsets, descriptor version 1, swizzle mode 4 = 64-byte swizzle).
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)4 << 61;
-  return d;
-}
-
-// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B,
-// A K-major, B K-major or MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// Byte offset of the 16-byte chunk `lc` of row `r` inside one 64-byte-swizzled
-// block whose rows are 64 bytes (the pattern TMA writes and the MMA reads).
-__device__ __forceinline__ uint32_t swz64(int r, int lc) {
-  return (uint32_t)(r * SW + ((lc ^ ((r >> 1) & 3)) << 4));
-}
 
 template <int D>
 struct PrefillCfg {
   static constexpr int CB = (D + SWE - 1) / SWE;    // 32-element column blocks
   static constexpr int Q_BYTES = CB * BM * SW;      // one head's Q tile
   static constexpr int KV_BYTES = CB * BN * SW;     // one K or V source tile
-  static constexpr int P_BYTES = (BN / SWE) * BM * SW;
 };
 
 struct PrefillParams {
@@ -645,37 +487,6 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
 
 // --- host side ---------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// 3-D bf16 map over rows of D elements: dims {D, rows, planes}, row stride
-// D*2 bytes, plane stride `plane_bytes`; box {32, box_rows, 1}, 64-byte swizzle.
-// Rows at or beyond `rows` read as zero.
-bool make_map(CUtensorMap* m, const void* base, int D, int rows, long long planes,
-              size_t plane_bytes, int box_rows) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)plane_bytes};
-  cuuint32_t box[3] = {(cuuint32_t)SWE, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int D, int NSRC, int G>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   PrefillMaps maps;
@@ -718,10 +529,11 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// two sources (fused); one source goes to the 128-key kernel
 template <int D>
-cudaError_t by_src(const PrefillArgs& a, cudaStream_t s) {
-  if (a.group == 1) return a.nsrc == 2 ? launch_t<D, 2, 1>(a, s) : launch_t<D, 1, 1>(a, s);
-  if (a.group == 2) return a.nsrc == 2 ? launch_t<D, 2, 2>(a, s) : launch_t<D, 1, 2>(a, s);
+cudaError_t by_group(const PrefillArgs& a, cudaStream_t s) {
+  if (a.group == 1) return launch_t<D, 2, 1>(a, s);
+  if (a.group == 2) return launch_t<D, 2, 2>(a, s);
   return cudaErrorNotSupported;
 }
 
@@ -729,11 +541,13 @@ cudaError_t by_src(const PrefillArgs& a, cudaStream_t s) {
 
 cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t stream) {
   if (a.batch * (long long)a.kv_heads > 65535 || a.S < 1) return cudaErrorNotSupported;
+  if (a.nsrc == 1) return prefill_wide_launch(a, stream);
+  if (a.nsrc != 2) return cudaErrorNotSupported;
   switch (a.head_dim) {
-    case 64: return by_src<64>(a, stream);
-    case 80: return by_src<80>(a, stream);
-    case 96: return by_src<96>(a, stream);
-    case 128: return by_src<128>(a, stream);
+    case 64: return by_group<64>(a, stream);
+    case 80: return by_group<80>(a, stream);
+    case 96: return by_group<96>(a, stream);
+    case 128: return by_group<128>(a, stream);
     default: return cudaErrorNotSupported;
   }
 }

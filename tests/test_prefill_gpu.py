@@ -111,6 +111,35 @@ def test_prefill_lengths_fused(S):
     s.close()
 
 
+@pytest.mark.parametrize("G", [1, 2])
+@pytest.mark.parametrize("S", [1, 2, 127, 128, 129, 255, 256, 257, 384, 513])
+def test_prefill_lengths_single_source(S, G):
+    """One-source layers run 128-key tiles with two 128-row groups per CTA
+    (two heads, or two row tiles of one head when G = 1): every length from
+    one row to several tiles with a ragged tail, both pairings."""
+    w = _w(64, G, 520)
+    s = PrefillSetup(w, 2, "vanilla", S, seed=20 + G)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "S=%d G=%d" % (S, G))
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    s.close()
+
+
+@pytest.mark.parametrize("mode", ["vanilla", "lite"])
+def test_prefill_group_one_window_chunks(mode):
+    """G = 1 with a sliding window and chunks starting off the tile grid: the
+    second row tile of a CTA starts 128 positions later than the first, so
+    its leading key tiles can lie wholly before its window."""
+    w = _w(128, 1, 700)
+    s = PrefillSetup(w, 4, mode, 700, seed=23, window=100)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "G=1 W=100 %s" % mode)
+    for a, c in ((0, 257), (257, 300), (557, 143)):
+        qc = s.q[:, :, a:a + c].contiguous()
+        oc = torch.empty_like(qc)
+        s.ctx.fkv_prefill_attn_chunk(qc, 4, mode, a, c, oc)
+        assert_close(f64(oc), _chunk_oracle(s, qc, a), "bf16", "G=1 chunk %d+%d" % (a, c))
+    s.close()
+
+
 @pytest.mark.parametrize("mode", ["lite", "fused"])
 def test_prefill_group_one(mode):
     w = _w(64, 1, 200)
