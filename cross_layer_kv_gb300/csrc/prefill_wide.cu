@@ -55,10 +55,13 @@ struct WideCfg {
   static constexpr int NS_FIT = (SMEM_LIMIT - 512 - FIXED) / STAGE;
   static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
   static constexpr int SOFTMAX_WARPS = 4 * NG;
-  // control warpgroup: TMA producer, MMA issuer and two idle warps (register
-  // reallocation works per warpgroup)
+  // control warpgroup: the TMA producer, one MMA-issuing warp per group and
+  // an idle warp (register reallocation works per warpgroup).  Each group has
+  // its own issuing thread: a thread that waits on an mbarrier right after
+  // issuing MMAs lets the tensor pipe run dry, and with two issuers the other
+  // group's products fill that gap.
   static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
-  static constexpr int MMA_WARP = PRODUCER_WARP + 1;
+  static constexpr int MMA_WARP = PRODUCER_WARP + 1;   // + g for group g
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);
   // registers per thread: 168 at launch (65536 / 384, in steps of 8); the
   // control warpgroup gives up to 56 and the softmax warpgroups take 224:
@@ -107,7 +110,8 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
   uint64_t* kv_empty = kv_full + NS;
   uint64_t* s_full = kv_empty + NS;   // [NG]
   uint64_t* p_full = s_full + NG;     // [NG]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_full + NG);
+  uint64_t* turn = p_full + NG;       // [NG]: group g may issue its next step
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(turn + NG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x;
@@ -145,11 +149,12 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
     mbar_init(q_ready, 128 * NG);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_empty[s], NG);   // one commit per group that reads the tile
     }
     for (int g = 0; g < NG; ++g) {
       mbar_init(&s_full[g], 1);
       mbar_init(&p_full[g], 128);
+      mbar_init(&turn[g], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -187,64 +192,81 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
         }
       }
     }
-  } else if (warp == C::MMA_WARP) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp < C::MMA_WARP + NG) {
+    // ---------------- MMA issuer of group g ----------------
+    const int g = warp - C::MMA_WARP;
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, true);
+      const uint32_t t_g = tmem + g * GROUP_COLS;
+      const uint32_t qbase = smem_u32(sQ + g * C::Q_BYTES);
       // S_g = Q_g K_j^T: M = 128 rows, N = 128 keys, K = D in steps of 16
-      auto issue_qk = [&](int g, int j) {
+      auto issue_qk = [&](int j) {
         const uint32_t kbase = smem_u32(stage_k(j % NS));
-        const uint32_t qbase = smem_u32(sQ + g * C::Q_BYTES);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (uint32_t)(k & 1) * 32;
           const uint64_t ad = sdesc(qbase + (k >> 1) * BM * SW + off, 16, 8 * SW);
           const uint64_t bd = sdesc(kbase + (k >> 1) * BN * SW + off, 16, 8 * SW);
-          mma_bf16(tmem + g * GROUP_COLS, ad, bd, IDESC_QK, k > 0);
+          mma_bf16(t_g, ad, bd, IDESC_QK, k > 0);
         }
       };
       // O_g += P_g V_j: A = P_g (bf16, two per column, in the first BN/2
       // columns of S_g), B = V_j as an MN-major operand, K = 128 keys
-      auto issue_pv = [&](int g, int j) {
+      auto issue_pv = [&](int j) {
         const uint32_t vbase = smem_u32(stage_v(j % NS));
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t bd = sdesc(vbase + k * 16 * SW, BN * SW, 8 * SW);
-          mma_bf16_ts(tmem + g * GROUP_COLS + BN, tmem + g * GROUP_COLS + k * 8, bd, IDESC_PV,
-                      (j > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts(t_g + BN, t_g + k * 8, bd, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
         }
       };
-      const int n0t = n_tiles(0), n1t = n_tiles(1);
-      bool ok = wait(scaled ? q_ready : bar_q, 0) && wait(&kv_full[0], 0);
+      // Step k of group g issues PV_g(k-1) (k > 0) and QK_g(k) (k < n_g).
+      // The two issuers take turns, group 0's step k before group 1's (the
+      // turn passes once a step's PV products are issued), so that the tensor
+      // pipe alternates between the groups and each group's softmax overlaps
+      // the other group's products (without the ordering the groups fall
+      // into step and their softmaxes run side by side).
+      // Group 1 of a one-head CTA may read one tile more than group 0 (its
+      // rows end 128 positions later): group 0 then passes the turn once
+      // more, and that last tile's slot is never refilled, so its kv_empty
+      // phase is never awaited.
+      const int ng = n_tiles(g);
+      auto take_turn = [&](int k) -> bool {
+        if (g == 0) return k == 0 || wait(&turn[0], (uint32_t)(k - 1) & 1u);
+        return wait(&turn[1], (uint32_t)k & 1u);
+      };
+      auto pass_turn = [&]() { mbar_arrive(&turn[1 - g]); };
+      bool ok = wait(scaled ? q_ready : bar_q, 0) && wait(&kv_full[0], 0) && take_turn(0);
       if (ok) {
         tc_fence_after();
-        for (int g = 0; g < NG; ++g) {
-          issue_qk(g, 0);
-          mma_commit(&s_full[g]);
-        }
+        issue_qk(0);
+        mma_commit(&s_full[g]);
+        pass_turn();
       }
-      for (int j = 0; ok && j < n_max; ++j) {
-        bool next_ready = false;
-        for (int g = 0; g < NG; ++g) {
-          const int ng = g == 0 ? n0t : n1t;
-          if (j >= ng) continue;
-          if (!wait(&p_full[g], (uint32_t)j & 1u)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(g, j);
-          if (j + 1 < ng) {
-            if (!next_ready) {
-              if (!wait(&kv_full[(j + 1) % NS], (uint32_t)((j + 1) / NS) & 1u)) { ok = false; break; }
-              tc_fence_after();
-              next_ready = true;
-            }
-            issue_qk(g, j + 1);
-          }
-          mma_commit(&s_full[g]);
+      for (int j = 0; ok && j < ng; ++j) {
+        // every wait comes before the step's first product, and the turn
+        // passes right after the PV products: a thread's mbarrier operation
+        // that follows its MMAs lets the pipe run dry unless the other issuer
+        // has products queued by then
+        const bool more = j + 1 < ng;
+        if (!wait(&p_full[g], (uint32_t)j & 1u) || !take_turn(j + 1) ||
+            (more && !wait(&kv_full[(j + 1) % NS], (uint32_t)((j + 1) / NS) & 1u))) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
+        tc_fence_after();
+        issue_pv(j);
+        pass_turn();
+        if (more) issue_qk(j + 1);
+        mma_commit(&s_full[g]);
         mma_commit(&kv_empty[j % NS]);
       }
+      if (g == 0)
+        for (int k = ng + 1; ok && k <= n_tiles(1); ++k) {
+          if (!take_turn(k)) break;
+          pass_turn();
+        }
     }
     }
   } else {
@@ -302,27 +324,35 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
       // lowest row-window start of the tile (warp-uniform)
       const bool diag = n0 + BN > pos_g || n0 + BN > S_kv || (W > 0 && n0 < pos_g + BM - W);
       if (diag) {
-        const int lo = W > 0 ? qpos - W + 1 : INT_MIN;
+        // visible keys of this row, as tile columns: lo <= c < hi
+        const int hi = min(qpos + 1, S_kv) - n0;
+        const int lo = W > 0 ? qpos - W + 1 - n0 : INT_MIN;
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const int kp = n0 + c;
-          if (kp > qpos || kp >= S_kv || kp < lo) sv[c] = -INFINITY;
-        }
+        for (int c = 0; c < BN; ++c)
+          if (c >= hi || c < lo) sv[c] = -INFINITY;
       }
-      // row max of the raw scores (the scale is positive, so it commutes)
-      float mx0 = fmax3f(sv[0], sv[1], sv[2]), mx1 = fmax3f(sv[3], sv[4], sv[5]);
+      // row max of the raw scores (the scale is positive, so it commutes):
+      // four independent chains over columns 8i .. 8i+7
+      float mx[4];
 #pragma unroll
-      for (int c = 6; c + 4 <= BN; c += 4) {
-        mx0 = fmax3f(mx0, sv[c], sv[c + 1]);
-        mx1 = fmax3f(mx1, sv[c + 2], sv[c + 3]);
+      for (int r = 0; r < 4; ++r) mx[r] = fmax3f(sv[2 * r], sv[2 * r + 1], sv[8 + 2 * r]);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) mx[r] = fmaxf(mx[r], sv[8 + 2 * r + 1]);
+#pragma unroll
+      for (int c = 16; c < BN; c += 8) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) mx[r] = fmax3f(mx[r], sv[c + 2 * r], sv[c + 2 * r + 1]);
       }
-      const float mt_row = fmax3f(mx0, mx1, fmaxf(sv[BN - 2], sv[BN - 1])) * p.scale_log2;
+      const float mt_row = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
       // Keep a stale max until it is exceeded by more than 2^8: P stays
       // below 256 (exact in bf16 and fp32) and O needs no rescaling.
       const float m_new = mt_row > m_run + RESCALE_SLACK ? mt_row : m_run;
       const float alpha = fast_exp2(m_run - m_new);
       const float neg_m = -m_new;
-      float ps0 = 0.f, ps1 = 0.f;
+      // row sum in four independent packed accumulators
+      float ps[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) ps[r] = 0.f;
       // P over the S tile just read, in quarters of 32 keys (16 columns)
 #pragma unroll
       for (int qt = 0; qt < 4; ++qt) {
@@ -334,12 +364,14 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
           float x0 = neg_m, x1 = neg_m;
           fma2(x0, x1, sv[cc], sv[cc + 1], p.scale_log2, p.scale_log2);
           const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-          add2(ps0, ps1, e0, e1);
+          const int r = (c >> 1) & 3;
+          add2(ps[2 * r], ps[2 * r + 1], e0, e1);
           __nv_bfloat162 v2 = __floats2bfloat162_rn(e0, e1);
           pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&v2));
         }
         tmem_st16(t_s + qt * 16, pk);
       }
+      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
         // O_g holds every PV product up to tile j-1 (s_full of tile j); the
         // next one is issued only after p_full below
@@ -353,7 +385,7 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
           tmem_st16(t_o + c, ov);
         }
       }
-      l_run = l_run * alpha + (ps0 + ps1);
+      l_run = l_run * alpha + psum;
       m_run = m_new;
       tmem_wait_st();
       tc_fence_before();
