@@ -110,8 +110,7 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
   uint64_t* kv_empty = kv_full + NS;
   uint64_t* s_full = kv_empty + NS;   // [NG]
   uint64_t* p_full = s_full + NG;     // [NG]
-  uint64_t* turn = p_full + NG;       // [NG]: group g may issue its next step
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(turn + NG);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_full + NG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x;
@@ -153,8 +152,9 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
     }
     for (int g = 0; g < NG; ++g) {
       mbar_init(&s_full[g], 1);
-      mbar_init(&p_full[g], 128);
-      mbar_init(&turn[g], 1);
+      // the group's 128 softmax threads, plus the other group's issuer once
+      // its previous step's PV products are queued (the turn)
+      mbar_init(&p_full[g], 129);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -226,31 +226,27 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
       // turn passes once a step's PV products are issued), so that the tensor
       // pipe alternates between the groups and each group's softmax overlaps
       // the other group's products (without the ordering the groups fall
-      // into step and their softmaxes run side by side).
+      // into step and their softmaxes run side by side).  The turn is one
+      // more arrival on the other group's p_full: phase j of p_full[g]
+      // completes when P_g(j) is in place and the other issuer has queued
+      // its step before (group 1's step j+1 follows group 0's, group 0's
+      // step j+1 follows group 1's step j), so one wait covers both.
       // Group 1 of a one-head CTA may read one tile more than group 0 (its
       // rows end 128 positions later): group 0 then passes the turn once
       // more, and that last tile's slot is never refilled, so its kv_empty
       // phase is never awaited.
       const int ng = n_tiles(g);
-      auto take_turn = [&](int k) -> bool {
-        if (g == 0) return k == 0 || wait(&turn[0], (uint32_t)(k - 1) & 1u);
-        return wait(&turn[1], (uint32_t)k & 1u);
-      };
-      auto pass_turn = [&]() { mbar_arrive(&turn[1 - g]); };
-      bool ok = wait(scaled ? q_ready : bar_q, 0) && wait(&kv_full[0], 0) && take_turn(0);
+      auto pass_turn = [&]() { mbar_arrive(&p_full[1 - g]); };
+      bool ok = wait(scaled ? q_ready : bar_q, 0) && wait(&kv_full[0], 0);
       if (ok) {
         tc_fence_after();
         issue_qk(0);
         mma_commit(&s_full[g]);
-        pass_turn();
+        if (g == 1) pass_turn();   // group 0's step 1 follows group 1's step 0
       }
       for (int j = 0; ok && j < ng; ++j) {
-        // every wait comes before the step's first product, and the turn
-        // passes right after the PV products: a thread's mbarrier operation
-        // that follows its MMAs lets the pipe run dry unless the other issuer
-        // has products queued by then
         const bool more = j + 1 < ng;
-        if (!wait(&p_full[g], (uint32_t)j & 1u) || !take_turn(j + 1) ||
+        if (!wait(&p_full[g], (uint32_t)j & 1u) ||
             (more && !wait(&kv_full[(j + 1) % NS], (uint32_t)((j + 1) / NS) & 1u))) {
           ok = false;
           break;
@@ -262,10 +258,13 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
         mma_commit(&s_full[g]);
         mma_commit(&kv_empty[j % NS]);
       }
+      // group 1 of a one-head CTA may take one step more than group 0: pass
+      // its turn too, once the phase before has completed (an early arrival
+      // would count towards that phase)
       if (g == 0)
-        for (int k = ng + 1; ok && k <= n_tiles(1); ++k) {
-          if (!take_turn(k)) break;
-          pass_turn();
+        for (int j = ng; ok && j < n_tiles(1); ++j) {
+          ok = wait(&p_full[1], (uint32_t)(j - 1) & 1u);
+          if (ok) pass_turn();
         }
     }
     }
