@@ -282,7 +282,13 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     // ---------------- fusion warpgroup (fused mode) ----------------
     if constexpr (NSRC == 2) {
       const int ft = tid - 32 * PL::SOFTMAX_WARPS;   // 0..127
-      constexpr int CHUNKS = CB * BN * (SW / 16);
+      // The thread's 16-byte chunks of a source tile are ft + 128 i: chunk i
+      // lies in column block i / 2 (a block holds BN rows of 4 chunks) and,
+      // the swizzle term being ((row >> 1) & 3) with row = ft / 4 + 32 i
+      // mod BN, always at the same logical chunk of its row.  So the thread
+      // needs the weights of one 8-column group per column block.
+      static_assert(BN * 4 == 256, "two chunks of a thread per column block");
+      const int lc = (ft & 3) ^ ((ft >> 3) & 3);
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % NS;
         if (!wait(&kv_full[s], (uint32_t)(j / NS) & 1u)) break;
@@ -292,33 +298,35 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
           const uint8_t* d1 = t == 0 ? stage_k(s, 1) : stage_v(s, 1);
           const float* w0 = sW + (t == 0 ? 0 : 2 * D);
           const float* w1 = sW + (t == 0 ? D : 3 * D);
-          for (int c = ft; c < CHUNKS; c += 128) {
-            const int cb = c / (BN * 4);
-            const int r = (c / 4) % BN;
-            const int lc = (c & 3) ^ ((r >> 1) & 3);
+#pragma unroll
+          for (int cb = 0; cb < CB; ++cb) {
             const int col = cb * SWE + lc * 8;
             if (col >= D) continue;  // padding columns stay zero
-            uint4* p0 = reinterpret_cast<uint4*>(d0 + (size_t)c * 16);
-            const uint4 x = *p0;
-            const uint4 y = *reinterpret_cast<const uint4*>(d1 + (size_t)c * 16);
-            const float4 wa = *reinterpret_cast<const float4*>(w0 + col);
-            const float4 wb = *reinterpret_cast<const float4*>(w0 + col + 4);
-            const float4 va = *reinterpret_cast<const float4*>(w1 + col);
-            const float4 vb = *reinterpret_cast<const float4*>(w1 + col + 4);
-            const float u0[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-            const float u1[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-            float fx[8], fy[8];
-            unpack16<__nv_bfloat16>(x, fx);
-            unpack16<__nv_bfloat16>(y, fy);
-            uint32_t o[4];
+            float2 u0[4], u1[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float lo = fmaf(u0[2 * e], fx[2 * e], u1[2 * e] * fy[2 * e]);
-              const float hi = fmaf(u0[2 * e + 1], fx[2 * e + 1], u1[2 * e + 1] * fy[2 * e + 1]);
-              __nv_bfloat162 v2 = __floats2bfloat162_rn(lo, hi);
-              o[e] = *reinterpret_cast<uint32_t*>(&v2);
+              u0[e] = *reinterpret_cast<const float2*>(w0 + col + 2 * e);
+              u1[e] = *reinterpret_cast<const float2*>(w1 + col + 2 * e);
             }
-            *p0 = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c = ft + 128 * (2 * cb + h);
+              uint4* p0 = reinterpret_cast<uint4*>(d0 + (size_t)c * 16);
+              const uint4 x = *p0;
+              const uint4 y = *reinterpret_cast<const uint4*>(d1 + (size_t)c * 16);
+              const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+              uint32_t o[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // a0 * x + a1 * y per channel pair: one packed multiply, one packed FMA
+                const float2 fx = make_float2(bf16lo(xw[e]), bf16hi(xw[e]));
+                const float2 fy = make_float2(bf16lo(yw[e]), bf16hi(yw[e]));
+                const float2 f = __ffma2_rn(u0[e], fx, __fmul2_rn(u1[e], fy));
+                __nv_bfloat162 v2 = __floats2bfloat162_rn(f.x, f.y);
+                o[e] = *reinterpret_cast<uint32_t*>(&v2);
+              }
+              *p0 = make_uint4(o[0], o[1], o[2], o[3]);
+            }
           }
         }
         fence_proxy_async_smem();
