@@ -91,7 +91,18 @@ struct PrefillPlan {
   static constexpr int FUSION_WARPS = NSRC == 2 ? 4 : 0;
   static constexpr int PRODUCER_WARP = SOFTMAX_WARPS + FUSION_WARPS;
   static constexpr int MMA_WARP = PRODUCER_WARP + 1;
-  static constexpr int THREADS = 32 * (MMA_WARP + 1);
+  // Two heads and two sources: 14 warps would cap every thread at 128
+  // registers (four warps on a scheduler).  Two idle warps complete the
+  // producer/MMA warpgroup, and register reallocation moves registers from
+  // it and the fusion warpgroup to the softmax warpgroups:
+  // 2 * 128 * 168 + 128 * 104 + 128 * 56 <= 512 * 128.
+  static constexpr bool SPLIT = NSRC == 2 && G == 2;
+  static constexpr int THREADS = 32 * (MMA_WARP + 1 + (SPLIT ? 2 : 0));
+  static constexpr int REGS_SOFTMAX = 168, REGS_FUSION = 104, REGS_CONTROL = 56;
+  static constexpr long long REGS_SPLIT = 4LL * G * 32 * REGS_SOFTMAX + 128LL * REGS_FUSION +
+                                          128LL * REGS_CONTROL;
+  static_assert(!SPLIT || (THREADS == 512 && REGS_SPLIT <= 512LL * 128),
+                "register split above the launch allocation");
   static_assert(NS >= 2, "shared memory too small for two K/V stages");
 };
 
@@ -202,6 +213,10 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if constexpr (PL::SPLIT) {
+    if (warp >= PL::PRODUCER_WARP)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PL::REGS_CONTROL));
+  }
   if (warp == PL::PRODUCER_WARP) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -278,9 +293,10 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
         mma_commit(&kv_empty[s]);
       }
     }
-  } else if (warp >= PL::SOFTMAX_WARPS) {
+  } else if (warp >= PL::SOFTMAX_WARPS && warp < PL::PRODUCER_WARP) {
     // ---------------- fusion warpgroup (fused mode) ----------------
     if constexpr (NSRC == 2) {
+      if constexpr (PL::SPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PL::REGS_FUSION));
       const int ft = tid - 32 * PL::SOFTMAX_WARPS;   // 0..127
       // The thread's 16-byte chunks of a source tile are ft + 128 i: chunk i
       // lies in column block i / 2 (a block holds BN rows of 4 chunks) and,
@@ -333,8 +349,9 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
         mbar_arrive(&kv_ready[s]);
       }
     }
-  } else {
+  } else if (warp < PL::SOFTMAX_WARPS) {
     // ---------------- softmax warpgroup of head hh ----------------
+    if constexpr (PL::SPLIT) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PL::REGS_SOFTMAX));
     const int hh = warp >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -532,6 +549,15 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   auto kern = prefill_kernel<D, NSRC, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  if (PrefillPlan<D, NSRC, G>::SPLIT) {
+    // the softmax warpgroups' register increase must fit the launch
+    // allocation, or it would never be granted: refuse instead
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if ((long long)fa.numRegs * PrefillPlan<D, NSRC, G>::THREADS < PrefillPlan<D, NSRC, G>::REGS_SPLIT)
+      return cudaErrorNotSupported;
+  }
   dim3 grid((unsigned)units, (unsigned)((a.S + BM - 1) / BM));
   kern<<<grid, PrefillPlan<D, NSRC, G>::THREADS, smem, stream>>>(maps, p);
   return cudaGetLastError();
