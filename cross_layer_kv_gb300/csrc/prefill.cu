@@ -314,6 +314,16 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
           const uint8_t* d1 = t == 0 ? stage_k(s, 1) : stage_v(s, 1);
           const float* w0 = sW + (t == 0 ? 0 : 2 * D);
           const float* w1 = sW + (t == 0 ? D : 3 * D);
+          // all of the thread's chunks of both sources first, so that no
+          // load waits behind the stores of an earlier chunk
+          constexpr int PER = 2 * CB;
+          uint4 xs[PER], ys[PER];
+#pragma unroll
+          for (int i = 0; i < PER; ++i) {
+            const int c = ft + 128 * i;
+            xs[i] = *reinterpret_cast<const uint4*>(d0 + (size_t)c * 16);
+            ys[i] = *reinterpret_cast<const uint4*>(d1 + (size_t)c * 16);
+          }
 #pragma unroll
           for (int cb = 0; cb < CB; ++cb) {
             const int col = cb * SWE + lc * 8;
@@ -326,10 +336,8 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const int c = ft + 128 * (2 * cb + h);
-              uint4* p0 = reinterpret_cast<uint4*>(d0 + (size_t)c * 16);
-              const uint4 x = *p0;
-              const uint4 y = *reinterpret_cast<const uint4*>(d1 + (size_t)c * 16);
+              const int i = 2 * cb + h;
+              const uint4 x = xs[i], y = ys[i];
               const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
               uint32_t o[4];
 #pragma unroll
@@ -341,7 +349,8 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
                 __nv_bfloat162 v2 = __floats2bfloat162_rn(f.x, f.y);
                 o[e] = *reinterpret_cast<uint32_t*>(&v2);
               }
-              *p0 = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(d0 + (size_t)(ft + 128 * i) * 16) =
+                  make_uint4(o[0], o[1], o[2], o[3]);
             }
           }
         }
