@@ -83,10 +83,17 @@ constexpr float RESCALE_SLACK = 8.f; // log2 growth of the running max tolerated
 template <int D, int NSRC, int G>
 struct PrefillPlan {
   using Cfg = PrefillCfg<D>;
-  static constexpr int STAGE = 2 * NSRC * Cfg::KV_BYTES;
+  static_assert(NSRC == 2, "one source runs the 128-key kernel");
+  // Two rings of 64-key slots: A holds the first source's K and V tile (the
+  // fused tiles are written over them, and the MMA commits free a slot), B
+  // the second source's (freed by the fusion warpgroup once it has read
+  // them, a period or more earlier)
+  static constexpr int SLOT = 2 * Cfg::KV_BYTES;
   static constexpr int FIXED = G * Cfg::Q_BYTES + 4 * D * 4 + AUX_BYTES + 512;
-  static constexpr int NS_FIT = (SMEM_LIMIT - FIXED) / STAGE;
-  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;   // K/V ring stages
+  static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / SLOT;
+  static constexpr int NB = SLOTS_FIT / 2 > 4 ? 4 : SLOTS_FIT / 2;
+  static constexpr int NA = SLOTS_FIT - NB > 4 ? 4 : SLOTS_FIT - NB;
+  static constexpr int NS = NA;
   static constexpr int SOFTMAX_WARPS = 4 * G;
   static constexpr int FUSION_WARPS = NSRC == 2 ? 4 : 0;
   static constexpr int PRODUCER_WARP = SOFTMAX_WARPS + FUSION_WARPS;
@@ -103,13 +110,13 @@ struct PrefillPlan {
                                           128LL * REGS_CONTROL;
   static_assert(!SPLIT || (THREADS == 512 && REGS_SPLIT <= 512LL * 128),
                 "register split above the launch allocation");
-  static_assert(NS >= 2, "shared memory too small for two K/V stages");
+  static_assert(NA >= 2 && NB >= 2, "shared memory too small for two slots per ring");
 };
 
 template <int D, int NSRC, int G>
 size_t prefill_smem_bytes() {
   using P = PrefillPlan<D, NSRC, G>;
-  size_t s = (size_t)P::FIXED + (size_t)P::NS * P::STAGE;
+  size_t s = (size_t)P::FIXED + (size_t)(P::NA + P::NB) * P::SLOT;
   // at least 116 KB so that one CTA holds an SM (it takes all 512 TMEM columns)
   return s < 118784 ? 118784 : s;
 }
@@ -118,10 +125,12 @@ size_t prefill_smem_bytes() {
 //   softmax warpgroups (one per head) | fusion warpgroup (fused mode) |
 //   TMA producer warp | MMA warp.
 // Pipeline per 64-key tile j, all hand-offs through mbarriers:
-//   producer:  kv_empty[s] -> TMA K/V sources -> kv_full[s]
-//   fusion:    kv_full[s] -> fused bf16 K/V written in place -> kv_ready[s]
+//   producer:  a_empty -> TMA first-source K/V -> a_full;
+//              b_empty -> TMA second-source K/V -> b_full
+//   fusion:    a_full, b_full -> fused bf16 K/V written over the first
+//              source's tiles -> b_empty, kv_ready
 //   MMA:       kv_ready[s] -> S_h[j%2] = Q_h K^T -> s_full[h][j%2];
-//              p_full[h] -> O_h += P_h V -> o_done[h]; then -> kv_empty[s]
+//              p_full[h] -> O_h += P_h V -> o_done[h]; then -> a_empty
 //              (S of tile j+1 is issued before waiting for P of tile j)
 //   softmax h: s_full -> row max / exp -> (o_done of tile j-1) -> rescale O
 //              in TMEM if the max grew by more than 2^8 -> P_h -> p_full[h]
@@ -130,20 +139,23 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillParams p) {
   using Cfg = PrefillCfg<D>;
   using PL = PrefillPlan<D, NSRC, G>;
-  constexpr int CB = Cfg::CB, NS = PL::NS;
+  constexpr int CB = Cfg::CB, NA = PL::NA, NB = PL::NB;
   extern __shared__ uint8_t smem_raw[];
   // 512-byte alignment: the period of the 64-byte swizzle pattern
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 511) &
                                              ~uintptr_t(511));
   uint8_t* sQ = smem;
   uint8_t* sKV = sQ + G * Cfg::Q_BYTES;
-  float* sW = reinterpret_cast<float*>(sKV + NS * PL::STAGE);
+  uint8_t* sB = sKV + NA * PL::SLOT;
+  float* sW = reinterpret_cast<float*>(sB + NB * PL::SLOT);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sW + 4 * D);
   uint64_t* bar_q = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_ready = kv_full + NS;
-  uint64_t* kv_empty = kv_ready + NS;
-  uint64_t* s_full = kv_empty + NS;     // [G][2]
+  uint64_t* a_full = bars + 1;          // [NA] first-source tiles landed
+  uint64_t* kv_ready = a_full + NA;     // [NA] fused tiles in place
+  uint64_t* a_empty = kv_ready + NA;    // [NA] MMA done with the slot
+  uint64_t* b_full = a_empty + NA;      // [NB] second-source tiles landed
+  uint64_t* b_empty = b_full + NB;      // [NB] fusion done with the slot
+  uint64_t* s_full = b_empty + NB;      // [G][2]
   uint64_t* p_full = s_full + 2 * G;    // [G]
   uint64_t* o_done = p_full + G;        // [G]
   uint64_t* q_ready = o_done + G;       // Q scaled by a (single-source scaled mode)
@@ -166,10 +178,11 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   const int ntiles = (min(pos0 + BM, S_kv) + BN - 1) / BN - j0;   // tiles processed
   const int H_q = p.H_kv * G;
 
-  auto stage_k = [&](int s, int src) { return sKV + (size_t)s * PL::STAGE + (size_t)src * Cfg::KV_BYTES; };
-  auto stage_v = [&](int s, int src) {
-    return sKV + (size_t)s * PL::STAGE + (size_t)(NSRC + src) * Cfg::KV_BYTES;
+  // key tile j: source src's K or V tile
+  auto stage_k = [&](int j, int src) {
+    return src == 0 ? sKV + (size_t)(j % NA) * PL::SLOT : sB + (size_t)(j % NB) * PL::SLOT;
   };
+  auto stage_v = [&](int j, int src) { return stage_k(j, src) + Cfg::KV_BYTES; };
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (*abort_flag) return false;
     if (mbar_wait_bounded(bar, parity)) return true;
@@ -180,10 +193,14 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&kv_full[s], 1);
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(&a_full[s], 1);
       mbar_init(&kv_ready[s], 128);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < NB; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 128);
     }
     for (int h = 0; h < G; ++h) {
       mbar_init(&s_full[2 * h], 1);
@@ -225,18 +242,32 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
         for (int cb = 0; cb < CB; ++cb)
           tma_load_3d(sQ + h * Cfg::Q_BYTES + cb * BM * SW, &maps.q, cb * SWE, m0,
                       b * H_q + kh * G + h, bar_q);
+      int issued = 0;   // copies issued: 2 per tile (ring A, then ring B)
       for (int j = 0; j < ntiles; ++j) {
-        const int s = j % NS, u = j / NS;
-        if (u > 0 && !wait(&kv_empty[s], (uint32_t)(u - 1) & 1u)) break;
         const int n0 = (j0 + j) * BN;
-        mbar_arrive_expect_tx(&kv_full[s], PL::STAGE);
+        if (j >= NA && !wait(&a_empty[j % NA], (uint32_t)(j / NA - 1) & 1u)) break;
+        mbar_arrive_expect_tx(&a_full[j % NA], PL::SLOT);
         for (int cb = 0; cb < CB; ++cb) {
-          tma_load_3d(stage_k(s, 0) + cb * BN * SW, &maps.k0, cb * SWE, n0, unit, &kv_full[s]);
-          tma_load_3d(stage_v(s, 0) + cb * BN * SW, &maps.v0, cb * SWE, n0, unit, &kv_full[s]);
-          if (NSRC == 2) {
-            tma_load_3d(stage_k(s, 1) + cb * BN * SW, &maps.k1, cb * SWE, n0, unit, &kv_full[s]);
-            tma_load_3d(stage_v(s, 1) + cb * BN * SW, &maps.v1, cb * SWE, n0, unit, &kv_full[s]);
-          }
+          tma_load_3d(stage_k(j, 0) + cb * BN * SW, &maps.k0, cb * SWE, n0, unit, &a_full[j % NA]);
+          tma_load_3d(stage_v(j, 0) + cb * BN * SW, &maps.v0, cb * SWE, n0, unit, &a_full[j % NA]);
+        }
+        issued = 2 * j + 1;
+        if (j >= NB && !wait(&b_empty[j % NB], (uint32_t)(j / NB - 1) & 1u)) break;
+        mbar_arrive_expect_tx(&b_full[j % NB], PL::SLOT);
+        for (int cb = 0; cb < CB; ++cb) {
+          tma_load_3d(stage_k(j, 1) + cb * BN * SW, &maps.k1, cb * SWE, n0, unit, &b_full[j % NB]);
+          tma_load_3d(stage_v(j, 1) + cb * BN * SW, &maps.v1, cb * SWE, n0, unit, &b_full[j % NB]);
+        }
+        issued = 2 * j + 2;
+      }
+      if (*abort_flag) {
+        // let this thread's copies still in flight land before the CTA exits
+        for (int i = max(0, issued - 2 * NA); i < issued; ++i) {
+          const int j = i >> 1;
+          if ((i & 1) == 0)
+            (void)mbar_wait_bounded(&a_full[j % NA], (uint32_t)(j / NA) & 1u, kDrainLimitNs);
+          else
+            (void)mbar_wait_bounded(&b_full[j % NB], (uint32_t)(j / NB) & 1u, kDrainLimitNs);
         }
       }
     }
@@ -245,10 +276,9 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, true);
-      uint64_t* ready = NSRC == 2 ? kv_ready : kv_full;
+      uint64_t* ready = kv_ready;
       auto issue_qk = [&](int j) {
-        const int s = j % NS;
-        const uint32_t kbase = smem_u32(stage_k(s, 0));
+        const uint32_t kbase = smem_u32(stage_k(j, 0));
         for (int h = 0; h < G; ++h) {
           const uint32_t qbase = smem_u32(sQ + h * Cfg::Q_BYTES);
 #pragma unroll
@@ -268,13 +298,11 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       }
       for (int j = 0; ok && j < ntiles; ++j) {
         if (j + 1 < ntiles) {
-          const int s1 = (j + 1) % NS;
-          if (!wait(&ready[s1], (uint32_t)((j + 1) / NS) & 1u)) break;
+          if (!wait(&ready[(j + 1) % NA], (uint32_t)((j + 1) / NA) & 1u)) break;
           tc_fence_after();
           issue_qk(j + 1);
         }
-        const int s = j % NS;
-        const uint32_t vbase = smem_u32(stage_v(s, 0));
+        const uint32_t vbase = smem_u32(stage_v(j, 0));
         for (int h = 0; h < G; ++h) {
           if (!wait(&p_full[h], (uint32_t)j & 1u)) { ok = false; break; }
           tc_fence_after();
@@ -290,7 +318,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
           mma_commit(&o_done[h]);
         }
         if (!ok) break;
-        mma_commit(&kv_empty[s]);
+        mma_commit(&a_empty[j % NA]);
       }
     }
   } else if (warp >= PL::SOFTMAX_WARPS && warp < PL::PRODUCER_WARP) {
@@ -306,12 +334,13 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       static_assert(BN * 4 == 256, "two chunks of a thread per column block");
       const int lc = (ft & 3) ^ ((ft >> 3) & 3);
       for (int j = 0; j < ntiles; ++j) {
-        const int s = j % NS;
-        if (!wait(&kv_full[s], (uint32_t)(j / NS) & 1u)) break;
+        if (!wait(&a_full[j % NA], (uint32_t)(j / NA) & 1u) ||
+            !wait(&b_full[j % NB], (uint32_t)(j / NB) & 1u))
+          break;
 #pragma unroll 1
         for (int t = 0; t < 2; ++t) {
-          uint8_t* d0 = t == 0 ? stage_k(s, 0) : stage_v(s, 0);
-          const uint8_t* d1 = t == 0 ? stage_k(s, 1) : stage_v(s, 1);
+          uint8_t* d0 = t == 0 ? stage_k(j, 0) : stage_v(j, 0);
+          const uint8_t* d1 = t == 0 ? stage_k(j, 1) : stage_v(j, 1);
           const float* w0 = sW + (t == 0 ? 0 : 2 * D);
           const float* w1 = sW + (t == 0 ? D : 3 * D);
           // all of the thread's chunks of both sources first, so that no
@@ -354,8 +383,9 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
             }
           }
         }
+        mbar_arrive(&b_empty[j % NB]);   // the second source's tiles are read
         fence_proxy_async_smem();
-        mbar_arrive(&kv_ready[s]);
+        mbar_arrive(&kv_ready[j % NA]);
       }
     }
   } else if (warp < PL::SOFTMAX_WARPS) {
@@ -508,10 +538,6 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag) {
-    // let the copies still in flight land before the CTA exits
-    for (int s = 0; s < NS && tid == 0; ++s) (void)mbar_wait_bounded(&kv_full[s], 0, kDrainLimitNs);
-  }
   if (warp == PL::MMA_WARP) {
     __syncwarp();
     tc_fence_after();
