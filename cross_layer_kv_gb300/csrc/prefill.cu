@@ -97,14 +97,15 @@ struct PrefillPlan {
   static constexpr int SOFTMAX_WARPS = 4 * G;
   static constexpr int FUSION_WARPS = NSRC == 2 ? 4 : 0;
   static constexpr int PRODUCER_WARP = SOFTMAX_WARPS + FUSION_WARPS;
-  static constexpr int MMA_WARP = PRODUCER_WARP + 1;
-  // Two heads and two sources: 14 warps would cap every thread at 128
-  // registers (four warps on a scheduler).  Two idle warps complete the
-  // producer/MMA warpgroup, and register reallocation moves registers from
-  // it and the fusion warpgroup to the softmax warpgroups:
-  // 2 * 128 * 168 + 128 * 104 + 128 * 56 <= 512 * 128.
+  // one MMA-issuing warp per head: a thread's mbarrier wait right after its
+  // MMAs lets the tensor pipe run dry, and the other head's products fill it
+  static constexpr int MMA_WARP = PRODUCER_WARP + 1;   // + h for head h
+  // Two heads: 15 warps would cap every thread at 128 registers (four warps
+  // on a scheduler).  An idle warp completes the producer/MMA warpgroup, and
+  // register reallocation moves registers from it and the fusion warpgroup
+  // to the softmax warpgroups: 2 * 128 * 168 + 128 * 104 + 128 * 56 <= 512 * 128.
   static constexpr bool SPLIT = NSRC == 2 && G == 2;
-  static constexpr int THREADS = 32 * (MMA_WARP + 1 + (SPLIT ? 2 : 0));
+  static constexpr int THREADS = 32 * (MMA_WARP + G + (SPLIT ? 1 : 0));
   static constexpr int REGS_SOFTMAX = 168, REGS_FUSION = 104, REGS_CONTROL = 56;
   static constexpr long long REGS_SPLIT = 4LL * G * 32 * REGS_SOFTMAX + 128LL * REGS_FUSION +
                                           128LL * REGS_CONTROL;
@@ -123,15 +124,16 @@ size_t prefill_smem_bytes() {
 
 // Warp-specialised CTA (G query heads of one KV head, 128 query rows each):
 //   softmax warpgroups (one per head) | fusion warpgroup (fused mode) |
-//   TMA producer warp | MMA warp.
+//   TMA producer warp | one MMA warp per head.
 // Pipeline per 64-key tile j, all hand-offs through mbarriers:
 //   producer:  a_empty -> TMA first-source K/V -> a_full;
 //              b_empty -> TMA second-source K/V -> b_full
 //   fusion:    a_full, b_full -> fused bf16 K/V written over the first
 //              source's tiles -> b_empty, kv_ready
-//   MMA:       kv_ready[s] -> S_h[j%2] = Q_h K^T -> s_full[h][j%2];
-//              p_full[h] -> O_h += P_h V -> o_done[h]; then -> a_empty
-//              (S of tile j+1 is issued before waiting for P of tile j)
+//   MMA of h:  kv_ready -> S_h[j%2] = Q_h K^T -> s_full[h][j%2];
+//              p_full[h] -> O_h += P_h V -> o_done[h], a_empty
+//              (one issuing warp per head; S of tile j+1 is issued before
+//              waiting for P of tile j)
 //   softmax h: s_full -> row max / exp -> (o_done of tile j-1) -> rescale O
 //              in TMEM if the max grew by more than 2^8 -> P_h -> p_full[h]
 template <int D, int NSRC, int G>
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     for (int s = 0; s < NA; ++s) {
       mbar_init(&a_full[s], 1);
       mbar_init(&kv_ready[s], 128);
-      mbar_init(&a_empty[s], 1);
+      mbar_init(&a_empty[s], G);   // one commit per head's issuer
     }
     for (int s = 0; s < NB; ++s) {
       mbar_init(&b_full[s], 1);
@@ -271,53 +273,49 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
         }
       }
     }
-  } else if (warp == PL::MMA_WARP) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp >= PL::MMA_WARP && warp < PL::MMA_WARP + G) {
+    // ---------------- MMA issuer of head h ----------------
+    const int h = warp - PL::MMA_WARP;
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, true);
-      uint64_t* ready = kv_ready;
+      const uint32_t qbase = smem_u32(sQ + h * Cfg::Q_BYTES);
       auto issue_qk = [&](int j) {
         const uint32_t kbase = smem_u32(stage_k(j, 0));
-        for (int h = 0; h < G; ++h) {
-          const uint32_t qbase = smem_u32(sQ + h * Cfg::Q_BYTES);
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (uint32_t)(k & 1) * 32;
-            const uint64_t ad = sdesc(qbase + (k >> 1) * BM * SW + off, 16, 8 * SW);
-            const uint64_t bd = sdesc(kbase + (k >> 1) * BN * SW + off, 16, 8 * SW);
-            mma_bf16(tmem + h * HEAD_COLS + (j & 1) * BN, ad, bd, IDESC_QK, k > 0);
-          }
-          mma_commit(&s_full[2 * h + (j & 1)]);
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (uint32_t)(k & 1) * 32;
+          const uint64_t ad = sdesc(qbase + (k >> 1) * BM * SW + off, 16, 8 * SW);
+          const uint64_t bd = sdesc(kbase + (k >> 1) * BN * SW + off, 16, 8 * SW);
+          mma_bf16(tmem + h * HEAD_COLS + (j & 1) * BN, ad, bd, IDESC_QK, k > 0);
         }
+        mma_commit(&s_full[2 * h + (j & 1)]);
       };
-      bool ok = wait(scaled ? q_ready : bar_q, 0) && wait(&ready[0], 0);
+      bool ok = wait(bar_q, 0) && wait(&kv_ready[0], 0);
       if (ok) {
         tc_fence_after();
         issue_qk(0);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
+        // S of tile j+1 goes to the other S buffer before P of tile j is awaited
         if (j + 1 < ntiles) {
-          if (!wait(&ready[(j + 1) % NA], (uint32_t)((j + 1) / NA) & 1u)) break;
+          if (!wait(&kv_ready[(j + 1) % NA], (uint32_t)((j + 1) / NA) & 1u)) break;
           tc_fence_after();
           issue_qk(j + 1);
         }
+        if (!wait(&p_full[h], (uint32_t)j & 1u)) break;
+        tc_fence_after();
+        // P_h (bf16, two per column) sits in the first BN/2 columns of the
+        // S tile it was computed from
         const uint32_t vbase = smem_u32(stage_v(j, 0));
-        for (int h = 0; h < G; ++h) {
-          if (!wait(&p_full[h], (uint32_t)j & 1u)) { ok = false; break; }
-          tc_fence_after();
-          // P_h (bf16, two per column) sits in the first BN/2 columns of the
-          // S tile it was computed from
-          const uint32_t ptmem = tmem + h * HEAD_COLS + (j & 1) * BN;
+        const uint32_t ptmem = tmem + h * HEAD_COLS + (j & 1) * BN;
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k) {
-            const uint64_t bd = sdesc(vbase + k * 16 * SW, BN * SW, 8 * SW);
-            mma_bf16_ts(tmem + h * HEAD_COLS + 2 * BN, ptmem + k * 8, bd, IDESC_PV,
-                        (j > 0 || k > 0) ? 1u : 0u);
-          }
-          mma_commit(&o_done[h]);
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t bd = sdesc(vbase + k * 16 * SW, BN * SW, 8 * SW);
+          mma_bf16_ts(tmem + h * HEAD_COLS + 2 * BN, ptmem + k * 8, bd, IDESC_PV,
+                      (j > 0 || k > 0) ? 1u : 0u);
         }
-        if (!ok) break;
+        mma_commit(&o_done[h]);
         mma_commit(&a_empty[j % NA]);
       }
     }
