@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
         for (int cb = 0; cb < CB; ++cb)
           tma_load_3d(sQ + g * C::Q_BYTES + cb * BM * SW, &maps.q, cb * SWE, g_row0(g),
                       b * H_q + g_head(g), bar_q);
+      int issued = 0;
       for (int j = 0; j < n_max; ++j) {
         const int s = j % NS, u = j / NS;
         if (u > 0 && !wait(&kv_empty[s], (uint32_t)(u - 1) & 1u)) break;
@@ -190,6 +191,12 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
           tma_load_3d(stage_k(s) + cb * BN * SW, &maps.k, cb * SWE, n0, unit, &kv_full[s]);
           tma_load_3d(stage_v(s) + cb * BN * SW, &maps.v, cb * SWE, n0, unit, &kv_full[s]);
         }
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        // let this thread's copies still in flight land before the CTA exits
+        for (int j = max(0, issued - NS); j < issued; ++j)
+          (void)mbar_wait_bounded(&kv_full[j % NS], (uint32_t)(j / NS) & 1u, kDrainLimitNs);
       }
     }
   } else if (warp < C::MMA_WARP + NG) {
@@ -421,12 +428,9 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
     }
   }
 
+  // (a producer that stopped early has let its copies in flight land)
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag) {
-    // let the copies still in flight land before the CTA exits
-    for (int s = 0; s < NS && tid == 0; ++s) (void)mbar_wait_bounded(&kv_full[s], 0, kDrainLimitNs);
-  }
   if (warp == C::MMA_WARP) {
     __syncwarp();
     tc_fence_after();
