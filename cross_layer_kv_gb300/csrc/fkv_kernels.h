@@ -106,8 +106,11 @@ struct PrefillArgs {
 
 // Returns cudaErrorNotSupported for shapes the tensor-core kernels do not
 // cover.  One source (nsrc = 1) runs the 128-key kernel of prefill_wide.cu;
-// two sources (fused) the 64-key kernel with in-place fusion of prefill.cu.
+// two sources (fused) with D <= 96 the 112-key kernel of
+// prefill_fused_wide.cu (Q in tensor memory), and with D = 128 the 64-key
+// kernel of prefill.cu.
 cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t prefill_wide_launch(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t prefill_fused_wide_launch(const PrefillArgs& a, cudaStream_t stream);
 
 }  // namespace fkv

@@ -610,6 +610,7 @@ cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t stream) {
   if (a.batch * (long long)a.kv_heads > 65535 || a.S < 1) return cudaErrorNotSupported;
   if (a.nsrc == 1) return prefill_wide_launch(a, stream);
   if (a.nsrc != 2) return cudaErrorNotSupported;
+  if (a.head_dim <= 96) return prefill_fused_wide_launch(a, stream);
   switch (a.head_dim) {
     case 64: return by_group<64>(a, stream);
     case 80: return by_group<80>(a, stream);
