@@ -1,26 +1,28 @@
-// Causal prefill attention for FusedKV upper layers (and the vanilla / Lite
-// paths) on the 5th-generation tensor cores of sm_103a.
+// Causal prefill attention for FusedKV upper layers with D = 128, on the
+// 5th-generation tensor cores of sm_103a, and the prefill entry point that
+// picks a kernel per call (one source: prefill_wide.cu; two sources with
+// D <= 96: prefill_fused_wide.cu).
 //
 // What one call computes: for every sequence b, query head h (KV head
 // kh = h / G) and query position m < S
 //     o_{h,m} = sum_{t <= m} softmax_t(scale * q_{h,m} . K_t) V_t
-// with K/V the layer's own cache (vanilla), K^n / V^1 (lite, FusedKV slides
-// Eq.(6)) or a_1 (.) K^1 + a_n (.) K^n and b_1 (.) V^1 + b_n (.) V^n (fused,
-// Eqs.(4)-(5)), built tile by tile in shared memory and never written to
-// global memory (Table 1 slide: fuse on demand; reading notes §2.3).
+// with K = a_1 (.) K^1 + a_n (.) K^n and V = b_1 (.) V^1 + b_n (.) V^n (FusedKV
+// slides Eqs.(4)-(5)), built tile by tile in shared memory and never written
+// to global memory (Table 1 slide: fuse on demand).
 //
 // Structure of one CTA: one 128-row query tile of one (b, kh) unit and all G
 // query heads of that KV head, with warps specialised by role:
 //  * a TMA producer warp (cp.async.bulk.tensor, 64-byte swizzle) loads the Q
-//    tiles once and the K/V source tiles of 64 keys into a ring of up to 4
-//    stages;
-//  * fused mode: a fusion warpgroup combines the two sources of each K and V
-//    tile in fp32 and writes the bf16 result in place, in the swizzled layout
-//    the tensor cores read (the fused tile serves all G heads);
-//  * an MMA warp issues tcgen05.mma: S_h = Q_h K^T into a double-buffered
-//    tensor-memory tile, and O_h += P_h V accumulated in tensor memory; the S
-//    of the next tile is issued before the P of this one is awaited, so the
-//    tensor cores work while the softmax warps run;
+//    tiles once and the source tiles of 64 keys into two rings: the first
+//    source's K and V (the fused tiles are written over them) and the
+//    second source's;
+//  * a fusion warpgroup combines the two sources of each K and V tile in
+//    fp32 and writes the bf16 result in place, in the swizzled layout the
+//    tensor cores read (the fused tile serves all G heads);
+//  * one MMA warp per head issues tcgen05.mma: S_h = Q_h K^T into a
+//    double-buffered tensor-memory tile, and O_h += P_h V accumulated in
+//    tensor memory; the S of the next tile is issued before the P of this one
+//    is awaited, so the tensor cores work while the softmax warps run;
 //  * one softmax warpgroup per head: each thread owns one query row (one TMEM
 //    lane), reads its S row with tcgen05.ld, applies the causal mask and the
 //    online (base-2) softmax and writes P_h (bf16) back over that S tile with
@@ -93,7 +95,6 @@ struct PrefillPlan {
   static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / SLOT;
   static constexpr int NB = SLOTS_FIT / 2 > 4 ? 4 : SLOTS_FIT / 2;
   static constexpr int NA = SLOTS_FIT - NB > 4 ? 4 : SLOTS_FIT - NB;
-  static constexpr int NS = NA;
   static constexpr int SOFTMAX_WARPS = 4 * G;
   static constexpr int FUSION_WARPS = NSRC == 2 ? 4 : 0;
   static constexpr int PRODUCER_WARP = SOFTMAX_WARPS + FUSION_WARPS;
@@ -160,8 +161,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   uint64_t* s_full = b_empty + NB;      // [G][2]
   uint64_t* p_full = s_full + 2 * G;    // [G]
   uint64_t* o_done = p_full + G;        // [G]
-  uint64_t* q_ready = o_done + G;       // Q scaled by a (single-source scaled mode)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + G);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x;
@@ -210,21 +210,14 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       mbar_init(&p_full[h], 128);
       mbar_init(&o_done[h], 1);
     }
-    mbar_init(q_ready, 128 * G);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // one source with channel weights: S = (Q (.) a) K^T, O = (P V) (.) b
-  const bool scaled = NSRC == 1 && p.a0 != nullptr;
-  if (NSRC == 2 || scaled) {
-    for (int i = tid; i < D; i += PL::THREADS) {
-      sW[i] = p.a0[kh * D + i];
-      sW[2 * D + i] = p.b0[kh * D + i];
-      if (NSRC == 2) {
-        sW[D + i] = p.a1[kh * D + i];
-        sW[3 * D + i] = p.b1[kh * D + i];
-      }
-    }
+  for (int i = tid; i < D; i += PL::THREADS) {
+    sW[i] = p.a0[kh * D + i];
+    sW[D + i] = p.a1[kh * D + i];
+    sW[2 * D + i] = p.b0[kh * D + i];
+    sW[3 * D + i] = p.b1[kh * D + i];
   }
   if (warp == PL::MMA_WARP) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
@@ -399,31 +392,6 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     const uint32_t t_o = t_head + 2 * BN;
     float m_run = -FLT_MAX, l_run = 0.f;
     bool ok = true;
-    if (scaled) {
-      // this thread's Q row of head hh times a, in place (swizzled chunks)
-      ok = wait(bar_q, 0);
-      uint8_t* qh = sQ + hh * Cfg::Q_BYTES;
-      for (int cb = 0; ok && cb < CB; ++cb) {
-        for (int lc = 0; lc < 4; ++lc) {
-          const int col = cb * SWE + lc * 8;
-          if (col >= D) continue;
-          uint4* pq = reinterpret_cast<uint4*>(qh + cb * BM * SW + swz64(row, lc));
-          float f[8];
-          unpack16<__nv_bfloat16>(*pq, f);
-          uint32_t o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(f[2 * e] * sW[col + 2 * e],
-                                                      f[2 * e + 1] * sW[col + 2 * e + 1]);
-            o[e] = *reinterpret_cast<uint32_t*>(&v2);
-          }
-          *pq = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(q_ready);
-      ok = __all_sync(0xffffffffu, ok);
-    }
     for (int j = 0; ok && j < ntiles; ++j) {
       const int n0 = (j0 + j) * BN;
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
@@ -515,10 +483,6 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
         float ov[16];
         tmem_ld16(t_o + c, ov);
         tmem_wait_ld();
-        if (scaled) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) ov[e] *= sW[2 * D + c + e];
-        }
         uint32_t q8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -556,13 +520,8 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
                      (size_t)a.S * D * 2, BM);
   ok = ok && make_map(&maps.k0, a.k[0], D, S_kv, units, kv_plane, BN);
   ok = ok && make_map(&maps.v0, a.v[0], D, S_kv, units, kv_plane, BN);
-  if (NSRC == 2) {
-    ok = ok && make_map(&maps.k1, a.k[1], D, S_kv, units, kv_plane, BN);
-    ok = ok && make_map(&maps.v1, a.v[1], D, S_kv, units, kv_plane, BN);
-  } else {
-    maps.k1 = maps.k0;
-    maps.v1 = maps.v0;
-  }
+  ok = ok && make_map(&maps.k1, a.k[1], D, S_kv, units, kv_plane, BN);
+  ok = ok && make_map(&maps.v1, a.v[1], D, S_kv, units, kv_plane, BN);
   if (!ok) return cudaErrorInvalidValue;
   PrefillParams p;
   p.a0 = a.a[0];
@@ -611,13 +570,8 @@ cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t stream) {
   if (a.nsrc == 1) return prefill_wide_launch(a, stream);
   if (a.nsrc != 2) return cudaErrorNotSupported;
   if (a.head_dim <= 96) return prefill_fused_wide_launch(a, stream);
-  switch (a.head_dim) {
-    case 64: return by_group<64>(a, stream);
-    case 80: return by_group<80>(a, stream);
-    case 96: return by_group<96>(a, stream);
-    case 128: return by_group<128>(a, stream);
-    default: return cudaErrorNotSupported;
-  }
+  if (a.head_dim == 128) return by_group<128>(a, stream);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace fkv

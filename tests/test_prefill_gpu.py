@@ -148,6 +148,33 @@ def test_prefill_group_one(mode):
     s.close()
 
 
+@pytest.mark.parametrize("G", [1, 2])
+def test_prefill_fused_head_dim_128(G):
+    """Fused layers with D = 128 run the 64-key kernel (the 112-key fused
+    kernel keeps Q in tensor memory, which does not fit at D = 128): both
+    pairings, several tiles and a ragged tail."""
+    w = _w(128, G, 330)
+    s = PrefillSetup(w, 4, "fused", 321, seed=30 + G)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "fused D=128 G=%d" % G)
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    s.close()
+
+
+@pytest.mark.parametrize("D", [64, 80, 96])
+def test_prefill_fused_group_one_window_chunks(D):
+    """The 112-key fused kernel with one head per KV head (two row tiles per
+    CTA), a sliding window and chunks that start off the tile grid."""
+    w = _w(D, 1, 600)
+    s = PrefillSetup(w, 4, "fused", 600, seed=40 + D, window=150)
+    assert_close(f64(s.run()), s.oracle(), "bf16", "fused G=1 W=150 D=%d" % D)
+    for a, c in ((0, 113), (113, 300), (413, 187)):
+        qc = s.q[:, :, a:a + c].contiguous()
+        oc = torch.empty_like(qc)
+        s.ctx.fkv_prefill_attn_chunk(qc, 4, "fused", a, c, oc)
+        assert_close(f64(oc), _chunk_oracle(s, qc, a), "bf16", "fused G=1 chunk %d+%d" % (a, c))
+    s.close()
+
+
 def test_prefill_storage_layer_and_untied():
     w = _w(128, 2, 190)
     s = PrefillSetup(w, 1, "fused", 190, seed=4)
