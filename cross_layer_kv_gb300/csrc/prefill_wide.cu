@@ -338,18 +338,17 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
           if (c >= hi || c < lo) sv[c] = -INFINITY;
       }
       // row max of the raw scores (the scale is positive, so it commutes):
-      // four independent chains over columns 8i .. 8i+7
-      float mx[4];
+      // eight independent chains over column pairs
+      float mx[8];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) mx[r] = fmax3f(sv[2 * r], sv[2 * r + 1], sv[8 + 2 * r]);
+      for (int r = 0; r < 8; ++r) mx[r] = fmaxf(sv[2 * r], sv[2 * r + 1]);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) mx[r] = fmaxf(mx[r], sv[8 + 2 * r + 1]);
+      for (int c = 16; c < BN; c += 16) {
 #pragma unroll
-      for (int c = 16; c < BN; c += 8) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) mx[r] = fmax3f(mx[r], sv[c + 2 * r], sv[c + 2 * r + 1]);
+        for (int r = 0; r < 8; ++r) mx[r] = fmax3f(mx[r], sv[c + 2 * r], sv[c + 2 * r + 1]);
       }
-      const float mt_row = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+      const float mt_row = fmaxf(fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]), mx[6]),
+                                 mx[7]) * p.scale_log2;
       // Keep a stale max until it is exceeded by more than 2^8: P stays
       // below 256 (exact in bf16 and fp32) and O needs no rescaling.
       const float m_new = mt_row > m_run + RESCALE_SLACK ? mt_row : m_run;
