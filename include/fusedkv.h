@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
   FKV_OK = 0,
   FKV_ERR_INVALID_ARG = 1,  /* bad pointer, size, layer, alignment or config */
-  FKV_ERR_UNSUPPORTED = 2,  /* valid request this build or config cannot serve */
+  FKV_ERR_UNSUPPORTED = 2,  /* valid request this library or config cannot serve */
   FKV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
   FKV_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out */
   FKV_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */

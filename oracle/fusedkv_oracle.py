@@ -17,7 +17,7 @@ Sources cited below (titles of the pages, then the section / equation / table):
 * [Notes] "FusedKV: 通过跨层融合重构 KV 缓存" -- reading notes on the same
   paper (sections 2.1-2.5 follow the paper's Sec.2).
 
-Readings of points the pages leave open (each is listed in the design doc):
+Readings of points the pages leave open:
 
 * layers are 1-based, L = 2n, storage layers 1..n, reconstruction layers
   n+1..L ([Notes] §2.1, Eq.(1));
@@ -298,7 +298,7 @@ def append_kv(cache: np.ndarray, new: np.ndarray, pos: Sequence[int]) -> np.ndar
 
 # ---------------------------------------------------------------------------
 # 4-bit KV cache ([Slides] "Four-bit KV quantization is the stronger
-# combination", Table 14).  KIVI's grouping is not on the pages; this build
+# combination", Table 14).  KIVI's grouping is not on the pages; this library
 # quantises each token row of each head in groups of Q4_GROUP channels with
 # an asymmetric uniform 4-bit code:
 #     min = min(x_g), scale = bf16((max(x_g) - min) / 15)   (fp32 division),

@@ -568,7 +568,7 @@ def test_window_prefill_matches_sdpa_band_mask():
 
 
 # --------------------------------------------------------------------------
-# 4-bit KV cache ([Slides] Table 14); the grouping is this build's reading
+# 4-bit KV cache ([Slides] Table 14); the grouping is this library's reading
 # --------------------------------------------------------------------------
 
 def test_bf16_round_matches_torch():
