@@ -229,57 +229,99 @@ __device__ __forceinline__ unsigned unit_arrive(unsigned long long* word, unsign
   return 0;
 }
 
-// Merge the partials of unit (b, h) -- written by warps wf..wl, skipping the
-// ones with empty ranges -- into the G output rows.  One warp; partials are
-// read through L2 (__ldcg), since other SMs wrote them in this launch.
-template <typename T, int D, int G>
+// Merge the partials of unit (b, h) -- written by warps wf..wl at slots
+// w + u, skipping the warps with empty ranges -- into the G output rows.  One
+// warp; partials are read through L2 (__ldcg), since other SMs wrote them in
+// this launch.  Lane i takes the (m, l) of partial i of a batch of 32, and
+// the o rows of MB partials (8, or fewer where registers are tight) are
+// loaded at once for all G heads, so a merge
+// of up to 32 partials costs two dependent L2 round trips rather than one per
+// partial and head.
+template <typename T, int D, int G, int MB = (G * ((D + 31) / 32) <= 4 ? 8 : 4)>
 __device__ __forceinline__ void merge_unit(const float* ws, T* out, long long u, long long wf,
                                            long long wl, long long N, long long total, int b,
                                            int h, int H, int lane) {
   constexpr int PS = partial_stride(D);
   constexpr int DPL = (D + 31) / 32;
-#pragma unroll 1
+  const float* base = ws + (size_t)(wf + u) * G * PS;
+  const int P = (int)(wl - wf + 1);
+  float M[G], L[G], acc[G][DPL];
+  float m0[G], l0[G];  // (m, l) of this lane's partial in the first batch
+#pragma unroll
   for (int hq = 0; hq < G; ++hq) {
-    float M = -FLT_MAX;
-    for (long long w0 = wf; w0 <= wl; w0 += 32) {
-      const long long w = w0 + lane;
-      if (w <= wl && w * total / N < (w + 1) * total / N)
-        M = fmaxf(M, __ldcg(ws + ((size_t)(w + u) * G + hq) * PS + D));
-    }
-    M = warp_max(M);
-    float L = 0.f;
-    float acc[DPL];
+    M[hq] = -FLT_MAX;
+    m0[hq] = -FLT_MAX;
+    l0[hq] = 0.f;
+  }
+  for (int p0 = 0; p0 < P; p0 += 32) {
+    const long long w = wf + p0 + lane;
+    if (p0 + lane < P && w * total / N < (w + 1) * total / N) {
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
-    for (long long w0 = wf; w0 <= wl; w0 += 32) {
-      const long long w = w0 + lane;
-      float sc = 0.f;
-      if (w <= wl && w * total / N < (w + 1) * total / N) {
-        const float* rec = ws + ((size_t)(w + u) * G + hq) * PS;
-        sc = exp2f(__ldcg(rec + D) - M);
-        L += sc * __ldcg(rec + D + 1);
+      for (int hq = 0; hq < G; ++hq) {
+        const float* rec = base + ((size_t)(p0 + lane) * G + hq) * PS;
+        const float mv = __ldcg(rec + D);
+        if (p0 == 0) {
+          m0[hq] = mv;
+          l0[hq] = __ldcg(rec + D + 1);
+        }
+        M[hq] = fmaxf(M[hq], mv);
       }
-      const int cnt = (int)min(32LL, wl - w0 + 1);
-#pragma unroll 1
-      for (int i = 0; i < cnt; ++i) {
-        const float si = __shfl_sync(0xffffffffu, sc, i);
-        if (si == 0.f) continue;
-        const float* rec = ws + ((size_t)(w0 + i + u) * G + hq) * PS;
+    }
+  }
 #pragma unroll
-        for (int k = 0; k < DPL; ++k) {
-          const int d = lane + 32 * k;
-          if (d < D) acc[k] = fmaf(si, __ldcg(rec + d), acc[k]);
+  for (int hq = 0; hq < G; ++hq) {
+    M[hq] = warp_max(M[hq]);
+    L[hq] = 0.f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[hq][k] = 0.f;
+  }
+  for (int p0 = 0; p0 < P; p0 += 32) {
+    const long long w = wf + p0 + lane;
+    const bool ok = p0 + lane < P && w * total / N < (w + 1) * total / N;
+    float sc[G];
+#pragma unroll
+    for (int hq = 0; hq < G; ++hq) {
+      sc[hq] = 0.f;
+      if (ok) {
+        const float* rec = base + ((size_t)(p0 + lane) * G + hq) * PS;
+        const float mv = p0 == 0 ? m0[hq] : __ldcg(rec + D);
+        const float lv = p0 == 0 ? l0[hq] : __ldcg(rec + D + 1);
+        sc[hq] = exp2f(mv - M[hq]);
+        L[hq] += sc[hq] * lv;
+      }
+    }
+    const int cnt = min(32, P - p0);
+#pragma unroll 1
+    for (int i0 = 0; i0 < cnt; i0 += MB) {
+#pragma unroll
+      for (int j = 0; j < MB; ++j) {
+        const int i = i0 + j;
+#pragma unroll
+        for (int hq = 0; hq < G; ++hq) {
+          const float si = __shfl_sync(0xffffffffu, sc[hq], i & 31);
+          const bool take = i < cnt && si != 0.f;
+          const float* rec = base + ((size_t)(p0 + i) * G + hq) * PS;
+#pragma unroll
+          for (int k = 0; k < DPL; ++k) {
+            const int d = lane + 32 * k;
+            float x = 0.f;
+            if (take && d < D) x = __ldcg(rec + d);
+            acc[hq][k] = fmaf(si, x, acc[hq][k]);
+          }
         }
       }
     }
-    const float inv = 1.f / warp_sum(L);
+  }
+#pragma unroll
+  for (int hq = 0; hq < G; ++hq) {
+    const float inv = 1.f / warp_sum(L[hq]);
     T* orow = out + ((size_t)b * H * G + (size_t)h * G + hq) * D;
 #pragma unroll
     for (int k = 0; k < DPL; ++k) {
       const int d = lane + 32 * k;
       if (d < D) {
-        if constexpr (sizeof(T) == 4) orow[d] = acc[k] * inv;
-        else orow[d] = __float2bfloat16_rn(acc[k] * inv);
+        if constexpr (sizeof(T) == 4) orow[d] = acc[hq][k] * inv;
+        else orow[d] = __float2bfloat16_rn(acc[hq][k] * inv);
       }
     }
   }
@@ -643,7 +685,9 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
       if (arrived == 0) flag_status(p.status, lane == 0 ? kDevTimeout : 0);
       if (arrived == (unsigned)need) {
         __threadfence();
-        merge_unit<T, D, G>(p.ws, static_cast<T*>(p.out), u, wf, wl, N, total, b, h, H, lane);
+        // (16-warp shapes have 128 registers a thread: two partials at a time)
+        merge_unit<T, D, G, (W > 8 ? 2 : (G * ((D + 31) / 32) <= 4 ? 8 : 4))>(
+            p.ws, static_cast<T*>(p.out), u, wf, wl, N, total, b, h, H, lane);
       }
     }
   }

@@ -75,6 +75,26 @@ def test_split_count_invariance(ctas):
     s.close()
 
 
+@pytest.mark.parametrize("ctas", [1, 3, 7])
+@pytest.mark.parametrize("mode", ["vanilla", "fused"])
+def test_many_short_units_per_cta(ctas, mode):
+    """Each CTA's range holds many short (b, kh) units, with empty sequences
+    between them: most warps draw no tile of most units and write weight-0
+    records, and units span CTA boundaries."""
+    w = _small(64, 2, S=300, Bt=16)
+    lens = [1, 0, 57, 300, 3, 0, 0, 120, 48, 49, 2, 0, 211, 96, 5, 17]
+    s = DecodeSetup(w, 4, [mode], seed=8, lens=lens, decode_ctas=ctas)
+    got = f64(s.run(mode))
+    # a length of 0 is flagged (and gives a zero row); the others are exact
+    assert s.ctx.fkv_get_device_status() == B.FKV_ERR_DEVICE_ARG
+    pairs = [(b, hq) for b in range(len(lens)) if lens[b] > 0 for hq in range(w.q_heads)]
+    want = s.oracle(mode, pairs)
+    assert_close(np.stack([got[b, hq] for b, hq in pairs]), want, "bf16",
+                 "ctas=%d %s" % (ctas, mode))
+    assert np.all(got[[b for b in range(len(lens)) if lens[b] == 0]] == 0)
+    s.close()
+
+
 def test_more_warps_than_rows():
     """A grid with more warps than cache rows (empty warp ranges)."""
     w = _small(64, 2, S=16, Bt=2)
