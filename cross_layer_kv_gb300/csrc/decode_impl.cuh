@@ -35,7 +35,8 @@
 //    rows, so one call is one kernel.  Arrivals are counted per unit in a
 //    64-bit word tagged with the call's epoch: a count left by an earlier call
 //    (or by a call that stopped early) carries another epoch and restarts, so
-//    the workspace never needs clearing.
+//    the workspace never needs clearing.  The merging warp clears its unit's
+//    word, so a launch replayed from a CUDA graph (same epoch) starts afresh.
 #pragma once
 
 #include <cfloat>
@@ -684,6 +685,9 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
       arrived = __shfl_sync(0xffffffffu, arrived, 0);
       if (arrived == 0) flag_status(p.status, lane == 0 ? kDevTimeout : 0);
       if (arrived == (unsigned)need) {
+        // No arrival of this call can follow: clear the word, so that a call
+        // with the same epoch (a CUDA graph replaying this launch) starts at 1.
+        if (lane == 0) p.counters[u] = 0ull;
         __threadfence();
         // (16-warp shapes have 128 registers a thread: two partials at a time)
         merge_unit<T, D, G, (W > 8 ? 2 : (G * ((D + 31) / 32) <= 4 ? 8 : 4))>(

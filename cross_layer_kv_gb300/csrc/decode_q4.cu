@@ -402,6 +402,9 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
       arrived = __shfl_sync(0xffffffffu, arrived, 0);
       if (arrived == 0) flag_status(p.status, lane == 0 ? kDevTimeout : 0);
       if (arrived == (unsigned)need) {
+        // No arrival of this call can follow: clear the word, so that a call
+        // with the same epoch (a CUDA graph replaying this launch) starts at 1.
+        if (lane == 0) p.counters[u] = 0ull;
         __threadfence();
         merge_unit<__nv_bfloat16, D, G>(p.ws, static_cast<__nv_bfloat16*>(p.out), u, wf, wl, N,
                                         total, b, h, H, lane);

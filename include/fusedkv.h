@@ -180,7 +180,10 @@ size_t fkv_decode_workspace_bytes(const fkv_ctx* ctx);
  * store_upper), FKV_LITE reads K^n and V^1, FKV_FUSED reads K^1, K^n, V^1, V^n
  * with the layer's weights and fuses them in registers, FKV_SCALED reads K^n
  * and V^1 scaled by a_first and b_first (sources as set by fkv_set_sources).
- * workspace: device, at least fkv_decode_workspace_bytes(ctx) bytes. */
+ * workspace: device, at least fkv_decode_workspace_bytes(ctx) bytes.
+ * The call launches one kernel on `stream` and makes no synchronising CUDA
+ * call, so it can be captured into a CUDA graph.  Every replay computes
+ * afresh: the kernel clears the arrival counts it used once it is done. */
 fkv_status fkv_decode_attn(fkv_ctx* ctx, const void* q, int layer, int mode,
                            const int32_t* seq_lens, void* out, void* workspace,
                            size_t workspace_bytes, void* stream);

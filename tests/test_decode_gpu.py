@@ -95,6 +95,30 @@ def test_many_short_units_per_cta(ctas, mode):
     s.close()
 
 
+@pytest.mark.parametrize("mode", ["vanilla", "fused"])
+def test_cuda_graph_replay(mode):
+    """A decode call captured in a CUDA graph is right on every replay, with
+    new queries each time.  A replay repeats the captured call's epoch, so the
+    unit arrival words must not carry a finished count from one replay into
+    the next."""
+    w = _small(64, 2, S=1500, Bt=3)
+    s = DecodeSetup(w, 4, [mode], seed=31, lens=[1500, 700, 33])
+    s.run(mode)  # an eager call first
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        s.ctx.fkv_decode_attn(s.q, s.layer, mode, s.lens, s.out, s.ws)
+    for i in range(3):
+        s.q.copy_(synth.make_query(w, s.layer, 100 + i, "cuda"))
+        s.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(f64(s.out), s.oracle(mode), "bf16", "replay %d %s" % (i, mode))
+    assert s.ctx.fkv_get_device_status() == B.FKV_OK
+    del g
+    s.close()
+
+
 def test_more_warps_than_rows():
     """A grid with more warps than cache rows (empty warp ranges)."""
     w = _small(64, 2, S=16, Bt=2)
