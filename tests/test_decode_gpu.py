@@ -119,6 +119,61 @@ def test_cuda_graph_replay(mode):
     s.close()
 
 
+def test_cuda_graph_decode_step_matches_eager():
+    """A whole decode step captured once in a CUDA graph and replayed gives,
+    bit for bit, what eager calls give on the same new rows and queries.
+    The step appends into the storage layers, then makes the storage-layer
+    calls and the fused upper-layer calls."""
+    w = _small(64, 2, S=600, Bt=2, L=4)  # storage layers 1-2, upper layers 3-4
+    L, n = w.num_layers, w.n
+    ctx = B.Context(L, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim, w.dtype)
+    caches = [synth.make_cache(w, l, 0, "cuda") for l in range(1, n + 1)]
+    for l, (k, v) in enumerate(caches, start=1):
+        ctx.fkv_bind_layer_cache(l, k, v)
+    for l in range(n + 1, L + 1):
+        ctx.fkv_set_fusion_weights(l, *synth.make_weights(w, l, 0, "cuda"))
+    lens = torch.tensor([600, 311], dtype=torch.int32, device="cuda")
+    pos = lens - 1
+    dt = ctx.torch_dtype
+    q = torch.empty(L, w.batch, w.q_heads, w.head_dim, dtype=dt, device="cuda")
+    kn = torch.empty(n, w.batch, w.kv_heads, 1, w.head_dim, dtype=dt, device="cuda")
+    vn = torch.empty_like(kn)
+    out = torch.empty_like(q)
+    ws = ctx.workspace("cuda")
+
+    def step():
+        for l in range(1, n + 1):
+            ctx.fkv_append_kv(l, kn[l - 1], vn[l - 1], pos, 1)
+        for l in range(1, L + 1):
+            ctx.fkv_decode_attn(q[l - 1], l, "fused" if l > n else "vanilla", lens, out[l - 1], ws)
+
+    def fill(seed):
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        for x in (q, kn, vn):
+            x.copy_(torch.randn(x.shape, generator=g, device="cuda").to(dt))
+
+    fill(1)
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=torch.cuda.Stream()):
+        step()
+    for seed in (2, 3, 4):
+        fill(seed)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        out.fill_(float("nan"))
+        step()
+        torch.cuda.synchronize()
+        assert not torch.isnan(got).any()
+        assert torch.equal(got, out), "replay with inputs %d" % seed
+    assert ctx.fkv_get_device_status() == B.FKV_OK
+    del graph
+    ctx.close()
+
+
 def test_more_warps_than_rows():
     """A grid with more warps than cache rows (empty warp ranges)."""
     w = _small(64, 2, S=16, Bt=2)
