@@ -183,7 +183,10 @@ size_t fkv_decode_workspace_bytes(const fkv_ctx* ctx);
  * workspace: device, at least fkv_decode_workspace_bytes(ctx) bytes.
  * The call launches one kernel on `stream` and makes no synchronising CUDA
  * call, so it can be captured into a CUDA graph.  Every replay computes
- * afresh: the kernel clears the arrival counts it used once it is done. */
+ * afresh: the kernel clears the arrival counts it used once it is done.  A
+ * replay that stopped early (FKV_ERR_TIMEOUT in the device status) can leave
+ * counts behind under the captured call's tag; zero the workspace before the
+ * next replay (a zero word is never a live count). */
 fkv_status fkv_decode_attn(fkv_ctx* ctx, const void* q, int layer, int mode,
                            const int32_t* seq_lens, void* out, void* workspace,
                            size_t workspace_bytes, void* stream);
