@@ -629,3 +629,52 @@ def test_q4_attention_is_attention_over_dequantised_caches():
     full = O.decode_attn(q, 3, L, O.FUSED, kc, vc, [S], weights=ws)
     # 4-bit noise, not a different function: close to the unquantised result
     assert np.max(np.abs(got - full)) < 0.2
+
+
+# Closed-form cases of the 4-bit quantiser, worked by hand from its stated
+# definition (min of the group; scale = bf16((max - min) / 15) with the
+# division in fp32; code = clamp(rint((x - min) / scale), 0, 15), rint rounding
+# halves to even).  [Slides] "Four-bit KV quantization is the stronger
+# combination", Table 14, names 4-bit KV caches; the grouping and code are
+# this library's reading.  Each case pins the step size: a divisor of 14 or
+# 16 in place of 15 changes the stored scale and at least one code.
+_Q4_CASES = [
+    # 0, 0.5, ..., 7.5: (7.5 - 0) / 15 = 0.5 exactly, codes 0..15
+    ("grid", [0.5 * j for j in range(16)], 0.5, 0.0, list(range(16))),
+    # span 30 from -10: scale 2.0; (x + 10) / 2 hits many halves, which
+    # round to even (7.5 -> 8, 0.5 -> 0, 14.5 -> 14, 5.5 -> 6, 6.5 -> 6,
+    # 8.5 -> 8, 9.5 -> 10, 10.5 -> 10)
+    ("ties", [-10, 20, 0, 5, -9, 19, 1, 2, 3, 4, 6, 7, 8, 9, 10, 11], 2.0, -10.0,
+     [0, 15, 5, 8, 0, 14, 6, 6, 6, 7, 8, 8, 9, 10, 10, 10]),
+    # span 1: 1/15 = 2^-4 * 1.0666..; to 8 significant bits 2^-4 * (1 + 9/128)
+    # = 0.06689453125.  x / scale: 1 -> 14.95, 0.5 -> 7.47, 0.25 -> 3.74,
+    # 0.75 -> 11.21, 0.125 -> 1.87, 0.375 -> 5.61, 0.625 -> 9.34, 0.875 -> 13.08
+    ("inexact", [0, 1, 0.5, 0.25, 0.75, 0.125, 0.375, 0.625, 0.875, 0, 1, 0.5, 0.25, 0.75,
+                 0.125, 0.375], 0.06689453125, 0.0,
+     [0, 15, 7, 4, 11, 2, 6, 9, 13, 0, 15, 7, 4, 11, 2, 6]),
+    # negative span 1.5 from -3: 0.1 in fp32 is 0x3DCCCCCD, which rounds up to
+    # the bf16 0x3DCD = 0.10009765625.  (x + 3) / scale: 1.5 -> 14.99,
+    # 0.75 -> 7.49, 1 -> 9.99, 0.5 -> 4.995, 1.25 -> 12.49, 0.25 -> 2.498,
+    # 1.375 -> 13.74
+    ("negative", [-3, -1.5, -2.25, -2, -2.5, -1.75, -2.75, -1.625, -3, -1.5, -2.25, -2, -2.5,
+                  -1.75, -2.75, -1.625], 0.10009765625, -3.0,
+     [0, 15, 7, 10, 5, 12, 2, 14, 0, 15, 7, 10, 5, 12, 2, 14]),
+]
+
+
+@pytest.mark.parametrize("name,x,scale,lo,codes", _Q4_CASES, ids=[c[0] for c in _Q4_CASES])
+def test_q4_quantiser_closed_form_cases(name, x, scale, lo, codes):
+    xs = np.asarray(x, dtype=np.float32)[None, :]
+    assert np.array_equal(O.bf16_round(xs), xs), "inputs must be bf16 values"
+    c, s, m = O.q4_quantize(xs)
+    assert float(s[0, 0]) == scale
+    assert float(m[0, 0]) == lo
+    assert c[0].tolist() == codes
+    # the group's max reconstructs within 15 bf16 ulps of the scale (the
+    # scale's own rounding, accumulated over the 15 steps)
+    ulp = 2.0 ** (np.floor(np.log2(scale)) - 7)
+    assert abs((lo + 15 * scale) - max(x)) <= 15 * ulp / 2 + 1e-12
+    # two groups side by side keep their own parameters
+    c2, s2, m2 = O.q4_quantize(np.concatenate([xs, xs[:, ::-1]], axis=1))
+    assert s2[0].tolist() == [scale, scale] and m2[0].tolist() == [lo, lo]
+    assert c2[0, 16:].tolist() == codes[::-1]
