@@ -19,7 +19,9 @@ struct fkv_ctx {
   float scale;    // softmax scale
   int device;
   int num_sms;
-  int* status;    // device status word
+  int* status;    // device words: the status (int32 at byte 0) and the
+                  // limit of the bounded waits in ns (uint64 at byte 8)
+  unsigned long long* wait_limit;
   std::vector<void*> k, v;                 // index: layer (1-based)
   std::vector<const float*> w[4];          // a_first, a_second, b_first, b_second
   std::vector<int> lite_src[2];            // lite / scaled sources: K, V
@@ -29,6 +31,11 @@ struct fkv_ctx {
 };
 
 namespace {
+
+// The device words of a context: status (int32) at byte 0, the limit of
+// the bounded waits (uint64, ns) at byte 8.
+constexpr size_t kDeviceWordsBytes = 16;
+constexpr unsigned long long kDefaultWaitLimitNs = fkv::kWaitLimitNs;
 
 // Process-wide call counter: tags each decode call's per-unit arrival counts
 // so that counts left in a reused workspace by earlier calls never match.
@@ -135,11 +142,56 @@ fkv::DecodeArgs decode_args(const fkv_ctx* c) {
   d.is_f32 = c->cfg.dtype == FKV_F32;
   d.softmax_scale = c->scale;
   d.status = c->status;
+  d.wait_limit = c->wait_limit;
   d.num_ctas = c->cfg.decode_ctas;
   return d;
 }
 
 }  // namespace
+
+namespace fkv {
+
+// One decode call after host validation (see fkv_decode_attn).  With
+// clear_counts the unit arrival words of this call's plan are zeroed on the
+// stream before the launch (the no-allocation entry point, whose caller
+// cannot reach its scratch array to clear it after a timed-out replay).
+fkv_status decode_attn_impl(fkv_ctx* c, const void* q, int layer, int mode,
+                            const int32_t* seq_lens, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream, bool clear_counts) {
+  if (!c) return FKV_ERR_INVALID_ARG;
+  fkv::DecodeArgs d = decode_args(c);
+  int q4 = 0;
+  fkv_status s = resolve_sources(c, layer, mode, d.k, d.v, d.a, d.b, &d.nsrc, &q4);
+  if (s != FKV_OK) return s;
+  if (!q || !out || !seq_lens || !aligned16(q) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return FKV_ERR_INVALID_ARG;
+  fkv::DecodePlan plan{};
+  const cudaError_t pe = q4 ? fkv::decode_q4_plan(d, c->num_sms, &plan)
+                            : fkv::decode_plan(d, c->num_sms, &plan);
+  if (pe != cudaSuccess) return FKV_ERR_UNSUPPORTED;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < plan.workspace_bytes)
+    return FKV_ERR_WORKSPACE;
+  d.q = q;
+  d.out = out;
+  d.seq_lens = seq_lens;
+  d.workspace = static_cast<float*>(workspace);
+  d.window = c->window[layer];
+  unsigned ep = g_decode_epoch.fetch_add(1);
+  if (ep == 0) ep = g_decode_epoch.fetch_add(1);
+  d.epoch = ep;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (clear_counts &&
+      cudaMemsetAsync(static_cast<char*>(workspace) + plan.partial_bytes, 0,
+                      plan.workspace_bytes - plan.partial_bytes, st) != cudaSuccess) {
+    cudaGetLastError();
+    return FKV_ERR_CUDA;
+  }
+  const cudaError_t e = q4 ? fkv::decode_q4_launch(d, plan, st) : fkv::decode_launch(d, plan, st);
+  return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
+}
+
+}  // namespace fkv
 
 extern "C" {
 
@@ -166,15 +218,20 @@ fkv_status fkv_create(const fkv_config* cfg, fkv_ctx** out) {
   c->fused_src[2].assign(cfg->num_layers + 1, 1);
   c->fused_src[3].assign(cfg->num_layers + 1, c->n);
   c->status = nullptr;
+  c->wait_limit = nullptr;
+  const unsigned long long limit = kDefaultWaitLimitNs;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
-      cudaMalloc(&c->status, sizeof(int)) != cudaSuccess ||
-      cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) {
+      cudaMalloc(&c->status, kDeviceWordsBytes) != cudaSuccess ||
+      cudaMemset(c->status, 0, kDeviceWordsBytes) != cudaSuccess ||
+      cudaMemcpy(reinterpret_cast<char*>(c->status) + 8, &limit, sizeof(limit),
+                 cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaGetLastError();
     if (c->status) cudaFree(c->status);
     delete c;
     return FKV_ERR_CUDA;
   }
+  c->wait_limit = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(c->status) + 8);
   *out = c;
   return FKV_OK;
 }
@@ -296,31 +353,8 @@ size_t fkv_decode_workspace_bytes(const fkv_ctx* c) {
 fkv_status fkv_decode_attn(fkv_ctx* c, const void* q, int layer, int mode,
                            const int32_t* seq_lens, void* out, void* workspace,
                            size_t workspace_bytes, void* stream) {
-  if (!c) return FKV_ERR_INVALID_ARG;
-  fkv::DecodeArgs d = decode_args(c);
-  int q4 = 0;
-  fkv_status s = resolve_sources(c, layer, mode, d.k, d.v, d.a, d.b, &d.nsrc, &q4);
-  if (s != FKV_OK) return s;
-  if (!q || !out || !seq_lens || !aligned16(q) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-    return FKV_ERR_INVALID_ARG;
-  fkv::DecodePlan plan{};
-  const cudaError_t pe = q4 ? fkv::decode_q4_plan(d, c->num_sms, &plan)
-                            : fkv::decode_plan(d, c->num_sms, &plan);
-  if (pe != cudaSuccess) return FKV_ERR_UNSUPPORTED;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < plan.workspace_bytes)
-    return FKV_ERR_WORKSPACE;
-  d.q = q;
-  d.out = out;
-  d.seq_lens = seq_lens;
-  d.workspace = static_cast<float*>(workspace);
-  d.window = c->window[layer];
-  unsigned ep = g_decode_epoch.fetch_add(1);
-  if (ep == 0) ep = g_decode_epoch.fetch_add(1);
-  d.epoch = ep;
-  const cudaError_t e = q4 ? fkv::decode_q4_launch(d, plan, static_cast<cudaStream_t>(stream))
-                           : fkv::decode_launch(d, plan, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
+  return fkv::decode_attn_impl(c, q, layer, mode, seq_lens, out, workspace, workspace_bytes,
+                               stream, false);
 }
 
 fkv_status fkv_prefill_attn(fkv_ctx* c, const void* q, int layer, int mode, int S, void* out,
@@ -345,6 +379,7 @@ fkv_status fkv_prefill_attn_chunk(fkv_ctx* c, const void* q, int layer, int mode
   p.q = q;
   p.out = out;
   p.status = c->status;
+  p.wait_limit = c->wait_limit;
   p.batch = c->cfg.batch;
   p.kv_heads = c->cfg.num_kv_heads;
   p.group = c->group;
@@ -371,6 +406,17 @@ fkv_status fkv_get_device_status(fkv_ctx* c, void* stream) {
       cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FKV_ERR_CUDA;
   return (h & fkv::kDevTimeoutBit) ? FKV_ERR_TIMEOUT : FKV_ERR_DEVICE_ARG;
+}
+
+fkv_status fkv_set_wait_limit(fkv_ctx* c, unsigned long long limit_ns) {
+  if (!c) return FKV_ERR_INVALID_ARG;
+  if (limit_ns > kDefaultWaitLimitNs) return FKV_ERR_INVALID_ARG;
+  if (cudaMemcpy(c->wait_limit, &limit_ns, sizeof(limit_ns), cudaMemcpyHostToDevice) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return FKV_ERR_CUDA;
+  }
+  return FKV_OK;
 }
 
 const char* fkv_status_string(fkv_status s) {

@@ -127,6 +127,7 @@ struct SplitParams {
   float* ws;                       // partials
   unsigned long long* counters;    // one arrival word per (b, kh) unit
   int* status;
+  const unsigned long long* wait_limit;  // limit of the bounded waits (device word)
   int B, H_kv, S_max;
   int window;                      // > 0: only the last `window` rows of each sequence
   unsigned epoch;                  // tag of this call's arrivals
@@ -359,6 +360,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
   }
   grid_dep_trigger();
   grid_dep_wait();
+  const unsigned long long wlim = wait_limit_ns(p.wait_limit);
 
   // Sequence lengths, clamped to [0, S_max]; one CTA reports bad ones.
   for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
@@ -513,10 +515,11 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
       fresh = false;
     }
 
-    if (!mbar_wait_bounded(&wbars[stage], parity)) {
+    if (!mbar_wait_bounded(&wbars[stage], parity, wlim)) {
       flag_status(p.status, kDevTimeout);
-      // Let the copies still in flight land before the CTA can exit.
-      for (int k = consumed + 1; k < issued; ++k)
+      // Let the copies still in flight land before the CTA can exit: every
+      // stage issued and not yet consumed, the one just awaited included.
+      for (int k = consumed; k < issued; ++k)
         (void)mbar_wait_bounded(&wbars[k % NS], (uint32_t)(k / NS) & 1u, kDrainLimitNs);
       return;
     }
@@ -722,6 +725,7 @@ cudaError_t decode_launch_t(const DecodeArgs& a, const DecodePlan& plan, cudaStr
   sp.counters = reinterpret_cast<unsigned long long*>(
       reinterpret_cast<char*>(a.workspace) + plan.partial_bytes);
   sp.status = a.status;
+  sp.wait_limit = a.wait_limit;
   sp.epoch = a.epoch;
   sp.B = a.batch;
   sp.H_kv = a.kv_heads;

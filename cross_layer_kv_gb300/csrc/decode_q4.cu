@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
   }
   grid_dep_trigger();
   grid_dep_wait();
+  const unsigned long long wlim = wait_limit_ns(p.wait_limit);
 
   for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
     int L = p.seq_lens[i];
@@ -234,9 +235,10 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
       fresh = false;
     }
 
-    if (!mbar_wait_bounded(&wbars[stage], parity)) {
+    if (!mbar_wait_bounded(&wbars[stage], parity, wlim)) {
       flag_status(p.status, kDevTimeout);
-      for (int k = consumed + 1; k < issued; ++k)
+      // let every stage issued and not yet consumed land, this one included
+      for (int k = consumed; k < issued; ++k)
         (void)mbar_wait_bounded(&wbars[k % NS], (uint32_t)(k / NS) & 1u, kDrainLimitNs);
       return;
     }
@@ -436,6 +438,7 @@ cudaError_t launch_q4(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t 
   sp.counters = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(a.workspace) +
                                                       plan.partial_bytes);
   sp.status = a.status;
+  sp.wait_limit = a.wait_limit;
   sp.epoch = a.epoch;
   sp.B = a.batch;
   sp.H_kv = a.kv_heads;

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "fkv_kernels.h"
+
 namespace fkv {
 
 // Bits of the device status word (one int32 per context).
@@ -15,9 +17,10 @@ enum : int {
   kDevTimeout = 2,   // a bounded wait ran out
 };
 
-// Wall-clock limit of every spin on an mbarrier.  Nothing legitimate waits
-// this long; a wait that runs out sets kDevTimeout and the kernel returns.
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+// kWaitLimitNs (fkv_kernels.h) is the default wall-clock limit of every spin
+// on an mbarrier.  Nothing legitimate waits that long; a wait that runs out
+// sets kDevTimeout and the kernel returns.  Draining copies already in flight
+// after such a timeout has its own limit:
 constexpr unsigned long long kDrainLimitNs = 50000000ull;   // 50 ms
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
@@ -44,6 +47,14 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 
 __device__ __forceinline__ void flag_status(int* status, int bit) {
   if (status) atomicOr(status, bit);
+}
+
+// The limit of the bounded waits of one launch.  Each context keeps it in a
+// device word beside its status word (kWaitLimitNs unless a test lowered it),
+// so that a launch replayed from a CUDA graph reads the current setting.
+// Read after grid_dep_wait().
+__device__ __forceinline__ unsigned long long wait_limit_ns(const unsigned long long* word) {
+  return word ? *word : kWaitLimitNs;
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -84,9 +95,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Spin until the phase with the given parity completes, or until `limit_ns`
-// of wall-clock time has passed.  Returns false on timeout.
+// of wall-clock time has passed.  Returns false on timeout.  A limit of 0
+// reports a timeout at once, without looking at the barrier: the failure
+// path's test setting (see wait_limit_ns above), which takes every kernel
+// down its timeout path at its first wait, whatever the timing.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns == 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {

@@ -6,7 +6,13 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/fusedkv.h"
+
 namespace fkv {
+
+// Default limit of every bounded device wait (a context's wait-limit word
+// starts here; only the failure-path tests lower it).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
 // One decode attention call, after host validation.  Pointers are device
 // pointers.  nsrc = 1: K from k[0], V from v[0] (vanilla or lite);
@@ -21,6 +27,7 @@ struct DecodeArgs {
   const int32_t* seq_lens;   // [B]
   float* workspace;          // split partials
   int* status;               // device status word
+  const unsigned long long* wait_limit;  // device word: limit of the bounded waits (ns)
   int batch, kv_heads, group, max_seq, head_dim;
   int nsrc;
   int is_f32;
@@ -97,6 +104,7 @@ struct PrefillArgs {
   const void* q;   // [B, H_q, S, D] bf16
   void* out;       // [B, H_q, S, D] bf16
   int* status;
+  const unsigned long long* wait_limit;  // device word: limit of the bounded waits (ns)
   int batch, kv_heads, group, max_seq, head_dim, S;
   int q_start;     // cache position of query row 0 (0 for a whole prompt)
   int window;      // > 0: sliding window of that many positions
@@ -112,5 +120,11 @@ struct PrefillArgs {
 cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t prefill_wide_launch(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t prefill_fused_wide_launch(const PrefillArgs& a, cudaStream_t stream);
+
+// The body of fkv_decode_attn (api.cu); clear_counts zeroes the call's unit
+// arrival words on the stream before the launch.  Internal to the library.
+__attribute__((visibility("hidden"))) fkv_status decode_attn_impl(
+    fkv_ctx* c, const void* q, int layer, int mode, const int32_t* seq_lens, void* out,
+    void* workspace, size_t workspace_bytes, void* stream, bool clear_counts);
 
 }  // namespace fkv

@@ -17,14 +17,19 @@
 // that device.  Make that first call before any stream capture.
 //
 // Every call shares the one array and it keeps the last call's contents.  The
-// kernels write every partial they read within the same call, so nothing in it
-// needs to start at zero.  Calls whose kernels overlap on the GPU (for example
-// on two streams without ordering between them) race on the array.
+// split partials are written before they are read within each call; the
+// per-unit arrival counts are the one part that must start at zero, and each
+// call clears them on its stream (one small cudaMemsetAsync) before its
+// kernel.  So a call after a replay that timed out, or after a call of
+// another context whose partials overlapped these counts, starts clean.
+// Calls whose kernels overlap on the GPU (for example on two streams without
+// ordering between them) race on the array.
 #include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "../../include/fusedkv.h"
+#include "fkv_kernels.h"
 
 namespace {
 
@@ -34,6 +39,10 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mutex;
+// Device address of the array, per device, looked up once per process.  A
+// device reset (cudaDeviceReset) ends the context that address belongs to;
+// this library is not meant to outlive one, and after it these cached
+// addresses would be stale.
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_decode_scratch on the current device (looked up once).
@@ -67,8 +76,8 @@ fkv_status fkv_decode_attn_noalloc(fkv_ctx* ctx, const void* q, int layer, int m
   void* scratch = nullptr;
   const fkv_status s = scratch_for_current_device(&scratch);
   if (s != FKV_OK) return s;
-  return fkv_decode_attn(ctx, q, layer, mode, seq_lens, out, scratch, kNoAllocScratchBytes,
-                         stream);
+  return fkv::decode_attn_impl(ctx, q, layer, mode, seq_lens, out, scratch,
+                              kNoAllocScratchBytes, stream, /*clear_counts=*/true);
 }
 
 }  // extern "C"

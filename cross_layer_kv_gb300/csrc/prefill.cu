@@ -65,6 +65,7 @@ struct PrefillParams {
   const float* b1;
   void* out;
   int* status;
+  const unsigned long long* wait_limit;  // limit of the bounded waits (device word)
   int B, H_kv;
   int S;        // query rows of this call (the chunk length C)
   int q_start;  // cache position of the first query row
@@ -161,8 +162,10 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   uint64_t* s_full = b_empty + NB;      // [G][2]
   uint64_t* p_full = s_full + 2 * G;    // [G]
   uint64_t* o_done = p_full + G;        // [G]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + G);
+  uint64_t* mma_drain = o_done + G;     // [G] an issuer's last products, after an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + G);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* sm_issued = reinterpret_cast<int*>(tmem_slot + 2);   // copies the producer issued
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -179,6 +182,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   const int j0 = W > 0 ? max(0, pos0 - W + 1) / BN : 0;
   const int ntiles = (min(pos0 + BM, S_kv) + BN - 1) / BN - j0;   // tiles processed
   const int H_q = p.H_kv * G;
+  const unsigned long long wlim = wait_limit_ns(p.wait_limit);
 
   // key tile j: source src's K or V tile
   auto stage_k = [&](int j, int src) {
@@ -187,7 +191,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   auto stage_v = [&](int j, int src) { return stage_k(j, src) + Cfg::KV_BYTES; };
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (*abort_flag) return false;
-    if (mbar_wait_bounded(bar, parity)) return true;
+    if (mbar_wait_bounded(bar, parity, wlim)) return true;
     *abort_flag = 1;
     flag_status(p.status, kDevTimeout);
     return false;
@@ -209,8 +213,10 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       mbar_init(&s_full[2 * h + 1], 1);
       mbar_init(&p_full[h], 128);
       mbar_init(&o_done[h], 1);
+      mbar_init(&mma_drain[h], 1);
     }
     *abort_flag = 0;
+    *sm_issued = 0;
     fence_mbar_init();
   }
   for (int i = tid; i < D; i += PL::THREADS) {
@@ -255,16 +261,7 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
         }
         issued = 2 * j + 2;
       }
-      if (*abort_flag) {
-        // let this thread's copies still in flight land before the CTA exits
-        for (int i = max(0, issued - 2 * NA); i < issued; ++i) {
-          const int j = i >> 1;
-          if ((i & 1) == 0)
-            (void)mbar_wait_bounded(&a_full[j % NA], (uint32_t)(j / NA) & 1u, kDrainLimitNs);
-          else
-            (void)mbar_wait_bounded(&b_full[j % NB], (uint32_t)(j / NB) & 1u, kDrainLimitNs);
-        }
-      }
+      *sm_issued = issued;
     }
   } else if (warp >= PL::MMA_WARP && warp < PL::MMA_WARP + G) {
     // ---------------- MMA issuer of head h ----------------
@@ -500,6 +497,28 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // A wait ran out somewhere, so no role may have awaited the last copies
+    // and products: the producer lets its copies in flight land (Q and the
+    // last tiles of each ring; an older tile was consumed before its slot was
+    // refilled) and each issuer lets its own products finish, before the CTA
+    // frees tensor memory and exits.
+    if (warp == PL::PRODUCER_WARP && lane == 0) {
+      (void)mbar_wait_bounded(bar_q, 0, kDrainLimitNs);
+      const int issued = *sm_issued;
+      const int ta = (issued + 1) / 2, tb = issued / 2;   // tiles issued per ring
+      for (int j = max(0, ta - NA); j < ta; ++j)
+        (void)mbar_wait_bounded(&a_full[j % NA], (uint32_t)(j / NA) & 1u, kDrainLimitNs);
+      for (int j = max(0, tb - NB); j < tb; ++j)
+        (void)mbar_wait_bounded(&b_full[j % NB], (uint32_t)(j / NB) & 1u, kDrainLimitNs);
+    }
+    if (warp >= PL::MMA_WARP && warp < PL::MMA_WARP + G && lane == 0) {
+      mma_commit(&mma_drain[warp - PL::MMA_WARP]);
+      (void)mbar_wait_bounded(&mma_drain[warp - PL::MMA_WARP], 0, kDrainLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == PL::MMA_WARP) {
     __syncwarp();
     tc_fence_after();
@@ -530,6 +549,7 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   p.b1 = a.b[1];
   p.out = a.out;
   p.status = a.status;
+  p.wait_limit = a.wait_limit;
   p.B = a.batch;
   p.H_kv = a.kv_heads;
   p.S = a.S;

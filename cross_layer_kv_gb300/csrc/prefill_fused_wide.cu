@@ -90,6 +90,7 @@ struct FwParams {
   const void* q;     // [B, H_q, S, D] bf16
   void* out;         // [B, H_q, S, D] bf16
   int* status;
+  const unsigned long long* wait_limit;  // limit of the bounded waits (device word)
   int H_kv, G;
   int S;        // query rows of this call (the chunk length C)
   int q_start;  // cache position of query row 0
@@ -129,8 +130,10 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
   uint64_t* step_ready = v1_empty + 4;   // [NSR]
   uint64_t* s_full = step_ready + NSR;   // [NG]
   uint64_t* p_full = s_full + NG;        // [NG]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_full + NG);
+  uint64_t* mma_drain = p_full + NG;     // [NG] an issuer's last products, after an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + NG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* sm_issued = reinterpret_cast<int*>(tmem_slot + 2);   // [2] copies each producer issued
   static_assert(NSK <= 4 && NSV <= 4 && NS1 <= 4, "barrier arrays hold 4 slots");
 
   const int tid = threadIdx.x;
@@ -151,6 +154,7 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
   const int j0 = W > 0 ? max(0, pos_first - W + 1) / BN : 0;
   auto n_tiles = [&](int g) { return (min(p.q_start + g_row0(g) + BM, S_kv) + BN - 1) / BN - j0; };
   const int n_max = max(n_tiles(0), n_tiles(1));
+  const unsigned long long wlim = wait_limit_ns(p.wait_limit);
 
   auto tile_k = [&](int j) { return sK + (size_t)(j % NSK) * C::KV_BYTES; };
   auto tile_v = [&](int j) { return sV + (size_t)(j % NSV) * C::KV_BYTES; };
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
   auto tile_v1 = [&](int j) { return sV1 + (size_t)(j % NS1) * C::KV_BYTES; };
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (*abort_flag) return false;
-    if (mbar_wait_bounded(bar, parity)) return true;
+    if (mbar_wait_bounded(bar, parity, wlim)) return true;
     *abort_flag = 1;
     flag_status(p.status, kDevTimeout);
     return false;
@@ -182,8 +186,10 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
       // the group's 128 softmax threads, plus the other group's issuer once
       // its previous step's PV products are queued (the turn)
       mbar_init(&p_full[g], 129);
+      mbar_init(&mma_drain[g], 1);
     }
     *abort_flag = 0;
+    sm_issued[0] = sm_issued[1] = 0;
     fence_mbar_init();
   }
   for (int i = tid; i < D; i += C::THREADS) {
@@ -301,16 +307,7 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
           tma_load_3d(d1 + cb * BN * SW, m1, cb * SWE, n0, unit, &f1[j % NS1]);
         issued = 2 * j + 2;
       }
-      if (*abort_flag) {
-        // let this thread's copies still in flight land before the CTA exits
-        for (int i = max(0, issued - 8); i < issued; ++i) {
-          const int j = i >> 1;
-          if ((i & 1) == 0)
-            (void)mbar_wait_bounded(&f0[j % n0s], (uint32_t)(j / n0s) & 1u, kDrainLimitNs);
-          else
-            (void)mbar_wait_bounded(&f1[j % NS1], (uint32_t)(j / NS1) & 1u, kDrainLimitNs);
-        }
-      }
+      sm_issued[is_k ? 0 : 1] = issued;
     } else if (warp >= C::MMA_WARP && warp < C::MMA_WARP + NG && lane == 0) {
       // ---------------- MMA issuer of group g ----------------
       const int g = warp - C::MMA_WARP;
@@ -533,6 +530,31 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
   // (a producer that stopped early has let its copies in flight land)
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // A wait ran out somewhere, so no role may have awaited the last copies
+    // and products: each TMA producer lets its copies in flight land (the
+    // last tiles of each of its rings; an older tile was consumed before its
+    // slot was refilled) and each issuer lets its own products finish,
+    // before the CTA frees tensor memory and exits.
+    if ((warp == C::K_PRODUCER_WARP || warp == C::V_PRODUCER_WARP) && lane == 0) {
+      const bool is_k = warp == C::K_PRODUCER_WARP;
+      const int n0s = is_k ? NSK : NSV;
+      uint64_t* f0 = is_k ? k_full : v_full;
+      uint64_t* f1 = is_k ? k1_full : v1_full;
+      const int issued = sm_issued[is_k ? 0 : 1];
+      const int t0 = (issued + 1) / 2, t1 = issued / 2;   // tiles issued per ring
+      for (int j = max(0, t0 - n0s); j < t0; ++j)
+        (void)mbar_wait_bounded(&f0[j % n0s], (uint32_t)(j / n0s) & 1u, kDrainLimitNs);
+      for (int j = max(0, t1 - NS1); j < t1; ++j)
+        (void)mbar_wait_bounded(&f1[j % NS1], (uint32_t)(j / NS1) & 1u, kDrainLimitNs);
+    }
+    if (warp >= C::MMA_WARP && warp < C::MMA_WARP + NG && lane == 0) {
+      mma_commit(&mma_drain[warp - C::MMA_WARP]);
+      (void)mbar_wait_bounded(&mma_drain[warp - C::MMA_WARP], 0, kDrainLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == C::MMA_WARP) {
     __syncwarp();
     tc_fence_after();
@@ -561,6 +583,7 @@ cudaError_t launch_fused_wide(const PrefillArgs& a, cudaStream_t stream) {
   p.q = a.q;
   p.out = a.out;
   p.status = a.status;
+  p.wait_limit = a.wait_limit;
   p.H_kv = a.kv_heads;
   p.G = a.group;
   p.S = a.S;

@@ -79,6 +79,7 @@ struct WideParams {
   const float* b;
   void* out;
   int* status;
+  const unsigned long long* wait_limit;  // limit of the bounded waits (device word)
   int H_kv, G;
   int S;        // query rows of this call (the chunk length C)
   int q_start;  // cache position of query row 0
@@ -110,8 +111,10 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
   uint64_t* kv_empty = kv_full + NS;
   uint64_t* s_full = kv_empty + NS;   // [NG]
   uint64_t* p_full = s_full + NG;     // [NG]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_full + NG);
+  uint64_t* mma_drain = p_full + NG;  // [NG] an issuer's last products, after an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + NG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* sm_issued = reinterpret_cast<int*>(tmem_slot + 2);   // K/V stages the producer issued
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -132,12 +135,13 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
   auto n_tiles = [&](int g) { return (min(p.q_start + g_row0(g) + BM, S_kv) + BN - 1) / BN - j0; };
   const int n_max = max(n_tiles(0), n_tiles(1));
   const bool scaled = p.a != nullptr;
+  const unsigned long long wlim = wait_limit_ns(p.wait_limit);
 
   auto stage_k = [&](int s) { return sKV + (size_t)s * C::STAGE; };
   auto stage_v = [&](int s) { return sKV + (size_t)s * C::STAGE + C::KV_BYTES; };
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (*abort_flag) return false;
-    if (mbar_wait_bounded(bar, parity)) return true;
+    if (mbar_wait_bounded(bar, parity, wlim)) return true;
     *abort_flag = 1;
     flag_status(p.status, kDevTimeout);
     return false;
@@ -155,8 +159,10 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
       // the group's 128 softmax threads, plus the other group's issuer once
       // its previous step's PV products are queued (the turn)
       mbar_init(&p_full[g], 129);
+      mbar_init(&mma_drain[g], 1);
     }
     *abort_flag = 0;
+    *sm_issued = 0;
     fence_mbar_init();
   }
   if (scaled) {
@@ -193,11 +199,7 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
         }
         issued = j + 1;
       }
-      if (*abort_flag) {
-        // let this thread's copies still in flight land before the CTA exits
-        for (int j = max(0, issued - NS); j < issued; ++j)
-          (void)mbar_wait_bounded(&kv_full[j % NS], (uint32_t)(j / NS) & 1u, kDrainLimitNs);
-      }
+      *sm_issued = issued;
     }
   } else if (warp < C::MMA_WARP + NG) {
     // ---------------- MMA issuer of group g ----------------
@@ -427,9 +429,27 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
     }
   }
 
-  // (a producer that stopped early has let its copies in flight land)
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // A wait ran out somewhere, so no role may have awaited the last copies
+    // and products: the producer lets its copies in flight land (Q and the
+    // last NS stages; every older stage was consumed before its slot was
+    // refilled) and each issuer lets its own products finish, before the CTA
+    // frees tensor memory and exits.
+    if (warp == C::PRODUCER_WARP && lane == 0) {
+      (void)mbar_wait_bounded(bar_q, 0, kDrainLimitNs);
+      const int issued = *sm_issued;
+      for (int j = max(0, issued - NS); j < issued; ++j)
+        (void)mbar_wait_bounded(&kv_full[j % NS], (uint32_t)(j / NS) & 1u, kDrainLimitNs);
+    }
+    if (warp >= C::MMA_WARP && warp < C::MMA_WARP + NG && lane == 0) {
+      mma_commit(&mma_drain[warp - C::MMA_WARP]);
+      (void)mbar_wait_bounded(&mma_drain[warp - C::MMA_WARP], 0, kDrainLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == C::MMA_WARP) {
     __syncwarp();
     tc_fence_after();
@@ -455,6 +475,7 @@ cudaError_t launch_wide(const PrefillArgs& a, cudaStream_t stream) {
   p.b = a.b[0];
   p.out = a.out;
   p.status = a.status;
+  p.wait_limit = a.wait_limit;
   p.H_kv = a.kv_heads;
   p.G = a.group;
   p.S = a.S;

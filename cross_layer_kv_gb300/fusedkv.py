@@ -80,6 +80,7 @@ _SIGS = {
     "fkv_prefill_attn_chunk": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int, _P, _P]),
     "fkv_get_device_status": (ctypes.c_int, [_P, _P]),
+    "fkv_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_ulonglong]),
     "fkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -305,3 +306,9 @@ class Context:
         """The device status code (FKV_OK, FKV_ERR_DEVICE_ARG, FKV_ERR_TIMEOUT);
         synchronises the stream and clears the word."""
         return int(self._lib.fkv_get_device_status(self.handle, _stream(stream)))
+
+    def fkv_set_wait_limit(self, limit_ns: int):
+        """Failure-path tests only: the limit of every bounded device wait of
+        this context's later kernels (1 s by default; 0 makes every wait
+        report a timeout at once).  Synchronous."""
+        _check(self._lib.fkv_set_wait_limit(self.handle, int(limit_ns)), "fkv_set_wait_limit")

@@ -36,7 +36,8 @@
  *     length out of range, a bounded wait that ran out) are recorded in a
  *     device status word read by fkv_get_device_status().
  *   - Nothing aborts, throws or allocates on the hot path; the library owns
- *     only its context (and, after fkv_create, one 4-byte device status word).
+ *     only its context (and, after fkv_create, 16 bytes of device words: the
+ *     status word and the limit of the bounded waits).
  */
 #ifndef FUSEDKV_H_
 #define FUSEDKV_H_
@@ -89,11 +90,12 @@ typedef struct fkv_ctx fkv_ctx;
 
 /* Create a context for the current CUDA device.  Validates the config
  * (FKV_ERR_INVALID_ARG / FKV_ERR_UNSUPPORTED before touching CUDA), then
- * queries the device and allocates the 4-byte status word (FKV_ERR_CUDA on
- * failure, e.g. no GPU).  *out is set to NULL on any error. */
+ * queries the device and allocates its 16 bytes of device words, the status
+ * word and the wait limit (FKV_ERR_CUDA on failure, e.g. no GPU).  *out is
+ * set to NULL on any error. */
 fkv_status fkv_create(const fkv_config* cfg, fkv_ctx** out);
 
-/* Free the context and its status word.  NULL is ignored.  Does not touch
+/* Free the context and its device words.  NULL is ignored.  Does not touch
  * caller buffers. */
 void fkv_destroy(fkv_ctx* ctx);
 
@@ -170,6 +172,14 @@ fkv_status fkv_append_kv(fkv_ctx* ctx, int layer, const void* k_new, const void*
 size_t fkv_decode_workspace_bytes(const fkv_ctx* ctx);
 
 /* One decode attention call of a layer (a single query position per sequence).
+ * What it computes: softmax attention of each query head over the layer's
+ * keys and values, where an upper layer's K/V are those of FusedKV slides
+ * "FusedKV learns two-source, channel-wise fusion", Eqs.(4)-(5) (fused) or
+ * "Lite separates the key source from the value source", Eq.(6) (lite),
+ * rebuilt on demand inside the kernel and never stored ("Half the storage can
+ * require 50% more cache I/O", Table 1: fused reads K^1, K^n, V^1, V^n, twice
+ * the bytes of a vanilla or lite call; reading notes §2.5 explains why decode
+ * can therefore be slower while storage halves).
  * q: device [B, H_q, D]; out: device [B, H_q, D]; both in the context dtype.
  * seq_lens: device int32 [B]; sequence b attends over cache rows
  * [0, seq_lens[b]) (the new token already appended).  A length outside
@@ -208,13 +218,23 @@ fkv_status fkv_decode_attn(fkv_ctx* ctx, const void* q, int layer, int mode,
  * 4 MiB gets FKV_ERR_WORKSPACE and nothing is launched.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  All calls
- * share the one array, and nothing in it needs to start at zero.  Calls whose
- * kernels overlap on the GPU (e.g. on unordered streams) race on it. */
+ * share the one array and it keeps the last call's contents.  The per-unit
+ * arrival counts are the only part that must start at zero: each call clears
+ * them on its stream (one cudaMemsetAsync of B * H_kv * 8 bytes) before its
+ * kernel, so a call that follows a timed-out one, or a call of another
+ * context whose partials overlapped these counts, starts clean.  Calls whose
+ * kernels overlap on the GPU (e.g. on unordered streams) race on the array.
+ * The address looked up is that of the device's current context; it is not
+ * looked up again after a device reset. */
 fkv_status fkv_decode_attn_noalloc(fkv_ctx* ctx, const void* q, int layer, int mode,
                                    const int32_t* seq_lens, void* out, void* stream);
 
 /* Causal prefill attention of a layer over a prompt occupying cache rows
  * [0, S) of every sequence (the storage caches already hold those rows).
+ * This is the attention kernel whose throughput and time to first token the
+ * FusedKV slides compare across methods ("Prefill improves while kernel
+ * throughput falls", Fig.4; reading notes §2.5); the upper layers' K/V follow
+ * Eqs.(4)-(6) as in fkv_decode_attn.
  * q: device [B, H_q, S, D]; out: device [B, H_q, S, D]; context dtype.
  * Query row m sees key rows t <= m.  Modes and sources as for decode; fused
  * K/V tiles are built while staging them for the tensor cores.
@@ -241,6 +261,18 @@ fkv_status fkv_prefill_attn_chunk(fkv_ctx* ctx, const void* q, int layer, int mo
  * FKV_OK, FKV_ERR_DEVICE_ARG or FKV_ERR_TIMEOUT (FKV_ERR_CUDA if the sync
  * itself fails). */
 fkv_status fkv_get_device_status(fkv_ctx* ctx, void* stream);
+
+/* For tests of the failure path only (the paper has no counterpart).  Sets
+ * the wall-clock limit, in ns, of every bounded device wait of this context's
+ * later kernels (fkv_create sets 1 s, the maximum accepted).  0 makes every
+ * wait report a timeout at once, which takes each kernel down its timeout
+ * path at its first wait, on a kernel that does no out-of-bounds access: it records
+ * FKV_ERR_TIMEOUT, lets its copies and products in flight finish (with their
+ * own fixed limit), frees its tensor memory and returns, leaving some outputs
+ * unwritten.  The limit lives in device memory, so replays of captured graphs
+ * read the current value.  Synchronous (cudaMemcpy): not during a stream
+ * capture.  FKV_ERR_INVALID_ARG above 1 s. */
+fkv_status fkv_set_wait_limit(fkv_ctx* ctx, unsigned long long limit_ns);
 
 /* A static, human-readable name of a status code. */
 const char* fkv_status_string(fkv_status s);
