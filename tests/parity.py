@@ -130,6 +130,27 @@ class DecodeSetup:
             out.append(o[0, 0])
         return np.stack(out)
 
+    def oracle_units(self, mode, units):
+        """float64 oracle outputs ``[len(units), G, D]``: all G query heads of
+        each listed (b, kv_head) unit, one oracle call per unit."""
+        import oracle as O
+        w = self.w
+        lens = self.lens.cpu().tolist()
+        G = w.group
+        sk = self.source_kwargs(mode)
+        sk["window"] = self.window
+        out = []
+        for b, kh in units:
+            n = lens[b]
+            kc = {l: f64(k[b:b + 1, kh:kh + 1, :n]) for l, (k, v) in self.caches.items()}
+            vc = {l: f64(v[b:b + 1, kh:kh + 1, :n]) for l, (k, v) in self.caches.items()}
+            ws = ({self.layer: tuple(f64(x[kh:kh + 1]) for x in self.weights)}
+                  if self.weights else None)
+            o = O.decode_attn(f64(self.q[b:b + 1, kh * G:(kh + 1) * G]), self.layer, w.num_layers,
+                              mode, kc, vc, [n], weights=ws, **sk)
+            out.append(o[0])
+        return np.stack(out)
+
     def close(self):
         self.ctx.close()
         self.caches.clear()

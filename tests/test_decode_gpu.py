@@ -243,24 +243,24 @@ def test_host_validation_launches_nothing():
 # full-size workloads, sampled rows
 # ---------------------------------------------------------------------------
 
-def _pairs(w, k, seed):
-    rng = np.random.default_rng(seed)
-    bs = rng.integers(0, w.batch, k)
-    hs = rng.integers(0, w.q_heads, k)
-    pairs = sorted(set(zip(bs.tolist(), hs.tolist())))
-    return pairs + [(0, 0), (w.batch - 1, w.q_heads - 1)]
+def _every_unit(w):
+    return [(b, kh) for b in range(w.batch) for kh in range(w.kv_heads)]
 
 
 @pytest.mark.parametrize("w", [synth.M332, synth.B1_5, synth.B4], ids=lambda w: w.name)
-@pytest.mark.parametrize("mode", MODES)
-def test_full_size_sampled(w, mode):
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_full_size_every_unit(w, mode):
+    """The benchmark's workloads in its launch configuration: every query
+    head of every (batch row, KV head) unit against the oracle, so that every
+    CTA position, stream-K boundary and merge of the timed launch is checked."""
     layer = w.num_layers  # the top reconstruction layer
     s = DecodeSetup(w, layer, [mode], seed=0)
     got = f64(s.run(mode))
     assert s.ctx.fkv_get_device_status() == B.FKV_OK
-    pairs = _pairs(w, 6, 11)
-    ref = s.oracle(mode, pairs)
-    sel = np.stack([got[b, h] for b, h in pairs])
+    G = w.group
+    units = _every_unit(w)
+    ref = s.oracle_units(mode, units)
+    sel = np.stack([got[b, kh * G:(kh + 1) * G] for b, kh in units])
     assert_close(sel, ref, "bf16", "%s %s" % (w.name, mode))
     s.close()
     torch.cuda.empty_cache()
@@ -270,9 +270,10 @@ def test_full_size_storage_layer():
     w = synth.M332
     s = DecodeSetup(w, 1, ["fused"], seed=0)
     got = f64(s.run("fused"))
-    pairs = _pairs(w, 4, 12)
-    assert_close(np.stack([got[b, h] for b, h in pairs]), s.oracle("fused", pairs), "bf16",
-                 "storage layer 1")
+    G = w.group
+    units = _every_unit(w)
+    assert_close(np.stack([got[b, kh * G:(kh + 1) * G] for b, kh in units]),
+                 s.oracle_units("fused", units), "bf16", "storage layer 1")
     s.close()
 
 
@@ -351,13 +352,14 @@ def test_window_decode(window, mode, D):
 
 @pytest.mark.parametrize("mode", MODES)
 def test_window_decode_full_size_332M(mode):
-    """332M workload with the pages' window of 512 (sampled rows)."""
+    """332M workload with the pages' window of 512 (every unit)."""
     w = synth.M332
     s = DecodeSetup(w, w.num_layers, [mode], seed=0, window=512)
     got = f64(s.run(mode))
-    pairs = _pairs(w, 6, 19)
-    assert_close(np.stack([got[b, h] for b, h in pairs]), s.oracle(mode, pairs), "bf16",
-                 "332M W=512 %s" % mode)
+    G = w.group
+    units = _every_unit(w)
+    assert_close(np.stack([got[b, kh * G:(kh + 1) * G] for b, kh in units]),
+                 s.oracle_units(mode, units), "bf16", "332M W=512 %s" % mode)
     s.close()
     torch.cuda.empty_cache()
 

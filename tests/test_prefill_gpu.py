@@ -203,17 +203,24 @@ def test_prefill_rejects():
     ctx.close()
 
 
+# Full-size checks: eight (batch row, query head) pairs that cover every batch
+# row, both heads of a KV head and both ends of the head range; in each, the
+# first and last row of every 128-row query tile.
+_FULL_PAIRS = [(0, 0), (0, 1), (1, 6), (1, 7), (2, 9), (2, 14), (3, 3), (3, 15)]
+_TILE_EDGES = sorted({r for t in range(8192 // 128) for r in (128 * t, 128 * t + 127)})
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_prefill_full_size_sampled(mode):
-    """650M-shaped workload (B=4, S=8192, 16/8 heads, D=96): sampled rows."""
+    """650M-shaped workload (B=4, S=8192, 16/8 heads, D=96): the first and
+    last row of every query tile of eight (b, h) pairs."""
     w = synth.M650_PREFILL
     s = PrefillSetup(w, w.num_layers, mode, w.seq, seed=0)
     got = f64(s.run())
     assert s.ctx.fkv_get_device_status() == B.FKV_OK
-    rows = [0, 1, 127, 128, 129, 4095, 8190, 8191]
-    for b, h in [(0, 0), (3, 15), (1, 6), (2, 9)]:
-        ref = s.oracle((b, h), rows=rows)
-        assert_close(got[b, h, rows], ref, "bf16", "650M %s b=%d h=%d" % (mode, b, h))
+    for b, h in _FULL_PAIRS:
+        ref = s.oracle((b, h), rows=_TILE_EDGES)
+        assert_close(got[b, h, _TILE_EDGES], ref, "bf16", "650M %s b=%d h=%d" % (mode, b, h))
     s.close()
     torch.cuda.empty_cache()
 
@@ -303,8 +310,8 @@ def test_prefill_chunk_full_size_sampled(mode):
     q_start = 4096
     s.ctx.fkv_prefill_attn_chunk(s.q, w.num_layers, mode, q_start, 4096, s.out)
     got = f64(s.out)
-    rows = [0, 1, 63, 64, 2047, 4095]
-    for b, h in [(0, 0), (3, 15), (2, 7)]:
+    rows = [r for r in _TILE_EDGES if r < 4096]
+    for b, h in _FULL_PAIRS:
         ref = _chunk_oracle(s, s.q, q_start, bh=(b, h), rows=rows)
         assert_close(got[b, h, rows], ref, "bf16", "650M chunk %s b=%d h=%d" % (mode, b, h))
     s.close()

@@ -193,3 +193,57 @@ def test_q4_rejects_mixed_formats_and_prefill():
                                    torch.zeros(1, 1, 8, 48, dtype=torch.uint8, device="cuda"))
     assert e.value.status == B.FKV_ERR_UNSUPPORTED
     cf.close()
+
+
+@pytest.mark.parametrize("mode", ["fused", "scaled"])
+def test_q4_decode_full_size_4B(mode):
+    """4B-shaped workload (B=4, S=131072, 32/16 heads, D=80) with 4-bit
+    source caches quantised by the oracle on the CPU one batch row at a time;
+    every (batch row, KV head) unit against the oracle over the dequantised
+    records."""
+    w = synth.B4
+    D, G, n = w.head_dim, w.group, w.n
+    layer = w.num_layers
+    ctx = B.Context(w.num_layers, w.batch, w.seq, w.q_heads, w.kv_heads, D, "bf16")
+    host = {}   # layer -> (k records, v records) as host uint8 arrays
+    keep = []
+    for l in sorted({1, n}):
+        k, v = synth.make_cache(w, l, 0, "cuda")
+        recs = []
+        for x in (k, v):
+            rec_h = np.empty((w.batch, w.kv_heads, w.seq, O.q4_row_bytes(D)), dtype=np.uint8)
+            for b in range(w.batch):
+                xb = x[b].to("cpu", torch.float32).numpy()
+                rec_h[b] = O.q4_pack(*O.q4_quantize(xb))
+            recs.append(rec_h)
+        del k, v
+        torch.cuda.empty_cache()
+        kr, vr = (torch.from_numpy(r).to("cuda") for r in recs)
+        ctx.fkv_bind_layer_cache_q4(l, kr, vr)
+        keep.append((kr, vr))
+        host[l] = tuple(recs)
+    wts = synth.make_weights(w, layer, 0, "cuda")
+    ctx.fkv_set_fusion_weights(layer, *wts)
+    q = synth.make_query(w, layer, 0, "cuda")
+    lens = synth.make_seq_lens(w, 0, "cuda")
+    out = torch.empty_like(q)
+    ctx.fkv_decode_attn(q, layer, mode, lens, out, ctx.workspace())
+    assert ctx.fkv_get_device_status() == B.FKV_OK
+    got = f64(out)
+    L = lens.cpu().tolist()
+    qh = f64(q)
+    wn = tuple(f64(x) for x in wts)
+    ref, sel = [], []
+    for b in range(w.batch):
+        for kh in range(w.kv_heads):
+            nb = L[b]
+            kc = {l: O.q4_dequantize_records(r[0][b:b + 1, kh:kh + 1, :nb], D) for l, r in host.items()}
+            vc = {l: O.q4_dequantize_records(r[1][b:b + 1, kh:kh + 1, :nb], D) for l, r in host.items()}
+            ws = {layer: tuple(x[kh:kh + 1] for x in wn)}
+            ref.append(O.decode_attn(qh[b:b + 1, kh * G:(kh + 1) * G], layer, w.num_layers, mode,
+                                     kc, vc, [nb], weights=ws)[0])
+            sel.append(got[b, kh * G:(kh + 1) * G])
+    assert_close(np.stack(sel), np.stack(ref), "bf16", "q4 4B %s" % mode)
+    ctx.close()
+    keep.clear()
+    torch.cuda.empty_cache()
