@@ -11,7 +11,13 @@ cached tokens per sequence), as the FusedKV Table 1 accounting counts it:
 `value` is fused-mode decode tokens/s (batch / step time) with every input
 resident in HBM; `modes` holds all three modes; `e2e` repeats the fused step
 through the same C-ABI calls with the per-step inputs copied from pinned host
-memory and the outputs read back inside the timed region.
+memory and the outputs read back inside the timed region.  The same step is
+timed on the 1.5B-shaped (24 layers, ragged lengths up to 32768) and 4B-shaped
+(36 layers, S=131072) workloads in every mode (`decode_steps_other_workloads`),
+beside the 650M causal prefill and the 4-bit decode calls; each section
+carries its own clock record.  `cpu_baseline` (and `--impl reference`) time
+the float64 oracle on whole fused steps, one single-threaded worker process
+per host core.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 (torchrun) every rank runs an independent replica (the path shards
@@ -22,7 +28,8 @@ from __future__ import annotations
 
 import os
 
-# The oracle baseline runs single-threaded so that `cores` is exact.
+# Each oracle worker process runs single-threaded (one per host core), so
+# that `cores` is exact.
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -133,6 +140,12 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class DecodeModel:
+    """Caches of every layer (so that vanilla can run), per-step inputs and
+    outputs of one attention-only decode step of a workload.  Sequences are
+    full (S rows) or, for ragged workloads, of their drawn lengths; each step
+    writes the new token at row len - 1 and attends over len rows, so the
+    step's shape stays fixed from step to step."""
+
     def __init__(self, w, device, seed=0):
         import cross_layer_kv_gb300 as fkv
         from cross_layer_kv_gb300 import synth
@@ -156,10 +169,9 @@ class DecodeModel:
         shape = (L, w.batch, w.kv_heads, 1, w.head_dim)
         self.k_new = torch.randn(shape, generator=g, device=device).to(w.torch_dtype)
         self.v_new = torch.randn(shape, generator=g, device=device).to(w.torch_dtype)
-        # every sequence is full: the new token is written at row S-1 and all
-        # S rows are attended (the step shape stays fixed from step to step)
-        self.pos = torch.full((w.batch,), w.seq - 1, dtype=torch.int32, device=device)
-        self.lens = torch.full((w.batch,), w.seq, dtype=torch.int32, device=device)
+        self.lens = synth.make_seq_lens(w, seed, device)
+        self.pos = (self.lens - 1).to(torch.int32)
+        self.rows = int(self.lens.sum())
         self.out = torch.empty_like(self.q)
         self.ws = self.ctx.workspace(device)
 
@@ -189,13 +201,14 @@ class DecodeModel:
         """Algorithmic cache bytes one decode call reads (K and V sources)."""
         w = self.w
         nsrc = 2 if (layer > w.n and mode == "fused") else 1
-        return 2 * nsrc * w.batch * w.kv_heads * w.seq * w.head_dim * w.elem_bytes
+        return 2 * nsrc * w.kv_heads * self.rows * w.head_dim * w.elem_bytes
 
     def step_bytes(self, mode):
         return sum(self.call_bytes(l, mode) for l in range(1, self.w.num_layers + 1))
 
     def close(self):
         self.ctx.close()
+        self.caches.clear()
 
 
 def _barrier(dist_on):
@@ -212,23 +225,31 @@ def _max_over_ranks(x, dist_on, device):
 
 
 def time_steps(model, mode, K, W, stream, dist_on, device, collect_upper=False):
+    """K steps after W warm-up steps, bracketed by barrier + synchronize; the
+    max over ranks of their CUDA-event time.  With collect_upper, a second
+    run of K steps records events around every upper-layer call (kept out of
+    the step timing, since an event between two calls breaks their
+    programmatic-dependent-launch overlap) and returns their mean duration."""
     for _ in range(W):
         model.step(mode, stream)
     torch.cuda.synchronize()
     _barrier(dist_on)
     torch.cuda.synchronize()
-    upper = [] if collect_upper else None
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        model.step(mode, stream, upper)
+        model.step(mode, stream)
     e1.record(stream)
     torch.cuda.synchronize()
     _barrier(dist_on)
     ms = _max_over_ranks(e0.elapsed_time(e1), dist_on, device)
     upper_ms = None
-    if upper:
+    if collect_upper:
+        upper = []
+        for _ in range(K):
+            model.step(mode, stream, upper)
+        torch.cuda.synchronize()
         upper_ms = statistics.fmean(a.elapsed_time(b) for a, b in upper)
     return ms, upper_ms
 
@@ -283,65 +304,175 @@ def time_e2e(model, K, W, stream, dist_on, device, graph=False):
 
 
 # ---------------------------------------------------------------------------
-# oracle timing (cpu_baseline and --impl reference)
+# oracle timing (cpu_baseline and --impl reference): whole attention-only
+# decode steps of the 332M workload in fused mode, the batch's sequences
+# spread over a spawn pool of one single-threaded process per host core
 # ---------------------------------------------------------------------------
 
-def oracle_decode_step_seconds(w, budget_s=12.0, seed=0):
-    """Time the float64 oracle on the attention-only fused decode step of
-    whole sequences (all 12 layers, one sequence at a time), as many
-    sequences as fit in about `budget_s` seconds.  Returns (s/token, sample)."""
+_ORACLE = {}
+
+
+def host_cores() -> int:
+    """Cores this process may run on (the affinity mask, else the CPU count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_worker_init(wname, seed):
+    """Pool initializer (untimed): one synthetic sequence of the workload --
+    the same recipe, seeded per worker -- as float64 arrays: the caches of the
+    storage layers, the fusion weights of the upper layers, a query per layer."""
     import oracle as O
     from cross_layer_kv_gb300 import synth
+    torch.set_num_threads(1)
+    w = synth.WORKLOADS[wname]
+    one = synth.Workload(w.name, w.num_layers, 1, w.seq, w.q_heads, w.kv_heads, w.head_dim,
+                         w.dtype)
+    seed = seed + 1000 * (os.getpid() % 1000)
     L, n = w.num_layers, w.n
-    one = synth.Workload(w.name, L, 1, w.seq, w.q_heads, w.kv_heads, w.head_dim, w.dtype)
-    caches, weights, qs = {}, {}, {}
+    kc, vc, weights, qs = {}, {}, {}, {}
     for l in range(1, n + 1):
         k, v = synth.make_cache(one, l, seed, "cpu")
-        caches[l] = (k.double().numpy(), v.double().numpy())
+        kc[l], vc[l] = k.double().numpy(), v.double().numpy()
     for l in range(n + 1, L + 1):
         weights[l] = tuple(x.double().numpy() for x in synth.make_weights(one, l, seed, "cpu"))
     for l in range(1, L + 1):
         qs[l] = synth.make_query(one, l, seed, "cpu").double().numpy()
-    kc = {l: c[0] for l, c in caches.items()}
-    vc = {l: c[1] for l, c in caches.items()}
-    seqs = 0
-    t0 = time.perf_counter()
-    while True:
-        for l in range(1, L + 1):
-            O.decode_attn(qs[l], l, L, O.FUSED, kc, vc, [w.seq], weights=weights)
-        seqs += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or seqs >= 64:
-            break
-    return el / seqs, "%d whole sequence(s) x %d layers, fused mode, S=%d, 1 thread" % (
-        seqs, L, w.seq)
+    _ORACLE.update(O=O, L=L, S=w.seq, kc=kc, vc=vc, weights=weights, qs=qs)
+
+
+def _oracle_sequence(_):
+    """The oracle's fused decode step of one sequence: all L layers in order."""
+    st = _ORACLE
+    O, L = st["O"], st["L"]
+    for l in range(1, L + 1):
+        O.decode_attn(st["qs"][l], l, L, O.FUSED, st["kc"], st["vc"], [st["S"]],
+                      weights=st["weights"])
+    return 1
+
+
+class OraclePool:
+    """A spawn pool (safe after CUDA initialisation) of host_cores() workers,
+    capped at the batch size; BLAS stays at one thread per process."""
+
+    def __init__(self, w, seed=0, workers=0):
+        import multiprocessing as mp
+        self.w = w
+        self.workers = max(1, min(workers or host_cores(), w.batch))
+        self.pool = mp.get_context("spawn").Pool(self.workers, initializer=_oracle_worker_init,
+                                                 initargs=(w.name, seed))
+
+    def step(self, rows):
+        """One step over `rows` sequences; returns its wall time in seconds."""
+        t0 = time.perf_counter()
+        done = sum(self.pool.map(_oracle_sequence, range(rows), chunksize=1))
+        assert done == rows
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def oracle_baseline(w, budget_s=4.0, workers=0):
+    """cpu_baseline leg: whole fused decode steps of the workload's batch on the
+    oracle pool, one warm-up step, then steps until `budget_s` of wall time."""
+    pool = OraclePool(w, workers=workers)
+    try:
+        pool.step(pool.workers)          # every worker built its inputs
+        pool.step(w.batch)               # warm-up step
+        steps, el = 0, 0.0
+        while el < budget_s or steps < 1:
+            el += pool.step(w.batch)
+            steps += 1
+    finally:
+        pool.close()
+    sample = ("%d whole fused decode step(s) of %d sequences x %d layers (S=%d) on %d "
+              "single-threaded worker processes, %.1f s wall" % (
+                  steps, w.batch, w.num_layers, w.seq, pool.workers, el))
+    return steps * w.batch / el, pool.workers, sample
+
+
+def workload_label(w) -> str:
+    """The config.workload string both arms report."""
+    return ("%s (%d layers, storage 1-%d, B=%d, S=%d, %d/%d heads, D=%d, %s), attention-only "
+            "decode step, fused mode" % (w.name, w.num_layers, w.n, w.batch, w.seq, w.q_heads,
+                                         w.kv_heads, w.head_dim, w.dtype))
 
 
 def run_reference(args, rank, dist_on):
+    """The reference arm: the oracle, as it stands, timing whole steps."""
     from cross_layer_kv_gb300 import synth
     w = synth.M332
     if rank != 0:
         return
-    per_tok = []
-    sample = ""
-    for _ in range(args.warmup):
-        oracle_decode_step_seconds(w, budget_s=0.0)
-    for _ in range(args.steps):
-        s, sample = oracle_decode_step_seconds(w, budget_s=args.ref_budget)
-        per_tok.append(s)
-    sec = statistics.fmean(per_tok)
-    val = 1.0 / sec
+    pool = OraclePool(w, workers=args.oracle_workers)
+    try:
+        pool.step(pool.workers)
+        rows = args.ref_rows or w.batch
+        t_full = pool.step(rows)                     # first warm-up step
+        # each step processes the whole batch unless K such steps would take
+        # more than ~150 s; then a bounded sample of the batch's sequences
+        if args.steps * t_full > 150.0:
+            rows = max(1, int(rows * 150.0 / (args.steps * t_full)))
+        for _ in range(args.warmup - 1):
+            pool.step(rows)
+        total = 0.0
+        for _ in range(args.steps):
+            total += pool.step(rows)
+    finally:
+        pool.close()
+    ms = total * 1e3 / args.steps
+    val = args.steps * rows / total
+    sample = ("%d steps of %d sequence(s) x %d layers (fused decode, S=%d) on %d single-"
+              "threaded worker processes" % (args.steps, rows, w.num_layers, w.seq, pool.workers))
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": sec * 1e3 * w.batch, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "global_batch": w.batch * args.gpus,
-                       "seq_len": w.seq, "parallelism": "replicas"},
-            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "config": {"workload": workload_label(w), "global_batch": w.batch * args.gpus,
+                       "seq_len": w.seq, "parallelism": "replicas" if args.gpus > 1 else "single",
+                       "rows_per_step": rows},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": pool.workers,
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def measure_modes(model, K, W, stream, dist_on, device, local, peaks, world):
+    """Decode steps of a model in each mode: tokens/s, step time and GB/s, and
+    the mean upper-layer call.  The clocks are sampled over the fused mode's
+    timed steps."""
+    w = model.w
+    modes = {}
+    clocks = None
+    for mode in ("vanilla", "lite", "fused"):
+        if mode == "fused":
+            with ClockSampler(local) as cs:
+                ms, up = time_steps(model, mode, K, W, stream, dist_on, device,
+                                    collect_upper=True)
+            clocks = cs.summary()
+        else:
+            ms, up = time_steps(model, mode, K, W, stream, dist_on, device, collect_upper=True)
+        step_ms = ms / K
+        gb = model.step_bytes(mode) / 1e9
+        ub = model.call_bytes(w.num_layers, mode) / 1e9
+        modes[mode] = {
+            "upper_call_us": up * 1e3,
+            "upper_call_GBps": ub / (up / 1e3),
+            "upper_call_pct_of_8TBps": 100.0 * ub / (up / 1e3) / HBM_REF_GBS,
+            "upper_call_pct_of_measured_hbm": 100.0 * ub / (up / 1e3) / peaks["hbm_gbs"],
+            "tokens_per_s": w.batch * world / (step_ms / 1e3),
+            "step_ms": step_ms,
+            "step_bytes_GB": gb,
+            "GBps": gb / (step_ms / 1e3),
+            "pct_of_8TBps": 100.0 * gb / (step_ms / 1e3) / HBM_REF_GBS,
+            "pct_of_measured_hbm": 100.0 * gb / (step_ms / 1e3) / peaks["hbm_gbs"],
+        }
+    return modes, clocks
 
 
 # ---------------------------------------------------------------------------
@@ -353,11 +484,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--ref-budget", type=float, default=4.0)
+    ap.add_argument("--cpu-budget", type=float, default=4.0,
+                    help="wall seconds of oracle steps for cpu_baseline (after a warm-up step)")
+    ap.add_argument("--ref-rows", type=int, default=0,
+                    help="sequences per reference step (0: the whole batch, unless K such "
+                         "steps would take over ~150 s)")
+    ap.add_argument("--oracle-workers", type=int, default=0,
+                    help="oracle worker processes (0: one per host core, at most the batch)")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-other-decode", action="store_true",
-                    help="skip the single-call timings of the 1.5B and 4B decode workloads")
+                    help="skip the decode steps of the 1.5B and 4B workloads and the 4-bit calls")
     ap.add_argument("--profile", default=None,
                     help="run one call type only, e.g. decode:fused:332M-decode, "
                          "decode:fused:332M-decode:q4 or prefill:fused:650M-prefill "
@@ -397,34 +533,9 @@ def main():
     peaks = _peaks()
     K, W = args.steps, args.warmup
 
-    modes = {}
-    clocks = None
-    upper_ms = None
-    launches = 0
-    for mode in ("vanilla", "lite", "fused"):
-        if mode == "fused":
-            with ClockSampler(local) as cs:
-                ms, up = time_steps(model, mode, K, W, stream, dist_on, device,
-                                    collect_upper=True)
-            clocks = cs.summary()
-            launches = K * model.launches_per_step(mode)
-            upper_ms = up
-        else:
-            ms, up = time_steps(model, mode, K, W, stream, dist_on, device, collect_upper=True)
-        step_ms = ms / K
-        gb = model.step_bytes(mode) / 1e9
-        ub = model.call_bytes(w.num_layers, mode) / 1e9
-        modes[mode] = {
-            "upper_call_us": up * 1e3,
-            "upper_call_GBps": ub / (up / 1e3),
-            "upper_call_pct_of_8TBps": 100.0 * ub / (up / 1e3) / HBM_REF_GBS,
-            "tokens_per_s": w.batch * world / (step_ms / 1e3),
-            "step_ms": step_ms,
-            "step_bytes_GB": gb,
-            "GBps": gb / (step_ms / 1e3),
-            "pct_of_8TBps": 100.0 * gb / (step_ms / 1e3) / HBM_REF_GBS,
-            "pct_of_measured_hbm": 100.0 * gb / (step_ms / 1e3) / peaks["hbm_gbs"],
-        }
+    modes, clocks = measure_modes(model, K, W, stream, dist_on, device, local, peaks, world)
+    launches = K * model.launches_per_step("fused")
+    upper_ms = modes["fused"]["upper_call_us"] / 1e3
 
     # dominant kernel: the fused upper-layer decode call
     call_bytes = model.call_bytes(w.num_layers, "fused")
@@ -457,17 +568,34 @@ def main():
 
     prefill = None
     if not args.no_prefill:
-        prefill = bench_prefill(device, stream, peaks, W)
+        with ClockSampler(local) as cs:
+            prefill = bench_prefill(device, stream, peaks, W)
+        prefill["clocks"] = cs.summary()
     other_decode = None
     q4 = None
     if not args.no_other_decode:
-        other_decode = bench_decode_calls(device, stream, peaks, W)
-        q4 = bench_q4_calls(device, stream, peaks, W)
+        other_decode = {}
+        for wo in (synth.B1_5, synth.B4):
+            m = DecodeModel(wo, device)
+            Ko = max(5, min(K, 20))
+            om, ocl = measure_modes(m, Ko, W, stream, dist_on, device, local, peaks, world)
+            other_decode[wo.name] = {
+                "workload": workload_label(wo).replace(", fused mode", ", each mode"),
+                "steps": Ko, "modes": om, "clocks": ocl,
+                "fused_over_vanilla_step_time": om["fused"]["step_ms"] / om["vanilla"]["step_ms"],
+                "lite_over_vanilla_step_time": om["lite"]["step_ms"] / om["vanilla"]["step_ms"]}
+            m.close()
+            del m
+            torch.cuda.empty_cache()
+        with ClockSampler(local) as cs:
+            q4 = bench_q4_calls(device, stream, peaks, W)
+        q4["clocks"] = cs.summary()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        sec, sample = oracle_decode_step_seconds(w, budget_s=args.cpu_budget)
-        cpu = {"value": 1.0 / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        val, cores, sample = oracle_baseline(w, budget_s=args.cpu_budget,
+                                             workers=args.oracle_workers)
+        cpu = {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": sample}
 
     fused = modes["fused"]
@@ -485,12 +613,12 @@ def main():
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name + " (12 layers, storage 1-6, B=32, S=8192, 16/8 heads, "
-                                   "D=64, bf16), attention-only decode step, fused mode",
+            "config": {"workload": workload_label(w),
                        "global_batch": w.batch * world, "seq_len": w.seq,
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (every call reads >= 0.5 GB)"},
             "modes": modes,
+            "fused_over_vanilla_step_time": modes["fused"]["step_ms"] / modes["vanilla"]["step_ms"],
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -500,7 +628,7 @@ def main():
         if prefill is not None:
             line["prefill"] = prefill
         if other_decode is not None:
-            line["decode_other_workloads"] = other_decode
+            line["decode_steps_other_workloads"] = other_decode
         if q4 is not None:
             line["decode_q4_332M"] = q4
         print(json.dumps(line), flush=True)
@@ -610,26 +738,6 @@ def bench_q4_calls(device, stream, peaks, W, reps=20):
         sc.close()
         del sc
         torch.cuda.empty_cache()
-    return res
-
-
-def bench_decode_calls(device, stream, peaks, W, reps=20):
-    """One upper-layer decode call per mode of the other decode workloads
-    (1.5B-shaped ragged, 4B-shaped 128k): time, GB/s, % of 8 TB/s."""
-    from cross_layer_kv_gb300 import synth
-    res = {}
-    for w in (synth.B1_5, synth.B4):
-        res[w.name] = {}
-        for mode in ("vanilla", "lite", "fused"):
-            sc = SingleCall("decode", mode, w, device, stream)
-            us = sc.time_us(stream, reps, W)
-            gbs = sc.bytes / (us * 1e-6) / 1e9
-            res[w.name][mode] = {"upper_call_us": us, "bytes": sc.bytes, "GBps": gbs,
-                                 "pct_of_8TBps": 100.0 * gbs / HBM_REF_GBS,
-                                 "pct_of_measured_hbm": 100.0 * gbs / peaks["hbm_gbs"]}
-            sc.close()
-            del sc
-            torch.cuda.empty_cache()
     return res
 
 

@@ -54,11 +54,15 @@ def test_reference_arm_under_torchrun_prints_once():
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
-           "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--ref-budget", "0.2"]
+           "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--ref-rows", "1",
+           "--oracle-workers", "1"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    # the timed region is K whole steps of the stated rows
+    assert d["config"]["rows_per_step"] == 1
+    assert abs(d["value"] - d["steps"] * 1 / (d["ms_per_step"] * d["steps"] / 1e3)) < 1e-6 * d["value"]
