@@ -20,9 +20,23 @@
 namespace fkv {
 namespace {
 
+// Launch shape (FKV_Q4_{WARPS,STAGES,STAGE_BYTES} override it at build time,
+// for tuning sweeps).
+#ifdef FKV_Q4_WARPS
+constexpr int Q4_W = FKV_Q4_WARPS;
+#else
 constexpr int Q4_W = 8;            // warps per CTA
-constexpr int Q4_NS = 3;           // ring stages per warp
-constexpr int Q4_SB = 8192;        // bytes per stage
+#endif
+#ifdef FKV_Q4_STAGES
+constexpr int Q4_NS = FKV_Q4_STAGES;
+#else
+constexpr int Q4_NS = 2;           // ring stages per warp
+#endif
+#ifdef FKV_Q4_STAGE_BYTES
+constexpr int Q4_SB = FKV_Q4_STAGE_BYTES;
+#else
+constexpr int Q4_SB = 12288;       // bytes per stage (larger tiles spread the per-tile work)
+#endif
 
 template <int D, int NSRC>
 struct Q4Cfg {

@@ -229,12 +229,15 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
             ys[i] = *reinterpret_cast<const uint4*>(d1 + (size_t)(cb * BN * 4 + q) * 16);
           }
         }
-        float2 u0[4], u1[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          u0[e] = *reinterpret_cast<const float2*>(w0 + col + 2 * e);
-          u1[e] = *reinterpret_cast<const float2*>(w1 + col + 2 * e);
-        }
+        // the block's 8 weights of each source, two 16-byte loads apiece
+        const float4 wa0 = *reinterpret_cast<const float4*>(w0 + col);
+        const float4 wa1 = *reinterpret_cast<const float4*>(w0 + col + 4);
+        const float4 wb0 = *reinterpret_cast<const float4*>(w1 + col);
+        const float4 wb1 = *reinterpret_cast<const float4*>(w1 + col + 4);
+        const float2 u0[4] = {make_float2(wa0.x, wa0.y), make_float2(wa0.z, wa0.w),
+                              make_float2(wa1.x, wa1.y), make_float2(wa1.z, wa1.w)};
+        const float2 u1[4] = {make_float2(wb0.x, wb0.y), make_float2(wb0.z, wb0.w),
+                              make_float2(wb1.x, wb1.y), make_float2(wb1.z, wb1.w)};
 #pragma unroll
         for (int i = 0; i < PER_BLOCK; ++i) {
           const int q = ft + 128 * i;
