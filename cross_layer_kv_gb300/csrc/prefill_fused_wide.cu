@@ -76,7 +76,13 @@ struct FwCfg {
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 8);
   // registers: 128 per thread at launch (65536 / 512); the control and
   // fusion warpgroups give some up and the softmax warpgroups take them
+#ifdef FKV_PFW_REGS_CONTROL
+  static constexpr int REGS_CONTROL = FKV_PFW_REGS_CONTROL;   // tuning sweeps
+  static constexpr int REGS_FUSION = FKV_PFW_REGS_FUSION;
+  static constexpr int REGS_SOFTMAX = FKV_PFW_REGS_SOFTMAX;
+#else
   static constexpr int REGS_CONTROL = 56, REGS_FUSION = 96, REGS_SOFTMAX = 176;
+#endif
   static constexpr long long REGS_SPLIT =
       (long long)NG * 128 * REGS_SOFTMAX + 128LL * REGS_CONTROL + 128LL * REGS_FUSION;
   static_assert(REGS_SPLIT <= (long long)THREADS * 128, "register split above the launch allocation");

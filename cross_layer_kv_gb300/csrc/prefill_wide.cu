@@ -66,8 +66,13 @@ struct WideCfg {
   // registers per thread: 168 at launch (65536 / 384, in steps of 8); the
   // control warpgroup gives up to 56 and the softmax warpgroups take 224:
   // 2 * 128 * 224 + 128 * 56 = 384 * 168, so the increase is always granted
+#ifdef FKV_PW_REGS_CONTROL
+  static constexpr int REGS_CONTROL = FKV_PW_REGS_CONTROL;   // tuning sweeps
+  static constexpr int REGS_SOFTMAX = FKV_PW_REGS_SOFTMAX;
+#else
   static constexpr int REGS_CONTROL = 56;
   static constexpr int REGS_SOFTMAX = 224;
+#endif
   static_assert(NG * 128 * REGS_SOFTMAX + 128 * REGS_CONTROL <= THREADS * 168,
                 "register split above the launch allocation");
   static constexpr size_t SMEM = 512 + (size_t)FIXED + (size_t)NS * STAGE;
