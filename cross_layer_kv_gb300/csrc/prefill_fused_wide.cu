@@ -21,10 +21,14 @@
 //    tiles are written over them and the MMA commits free a slot) and the
 //    second source's K and V (freed by the fusion warpgroup as soon as it has
 //    read them).
-//  * A fusion warpgroup combines the two sources of each tile in fp32 and
-//    writes bf16 over the first source's tile, in the swizzled layout the
-//    MMA reads.  Its step k fuses V_{k-1} and K_k, the tiles MMA step k reads,
-//    and signals one barrier per step.
+//  * A fusion warpgroup combines the two sources of each tile and writes
+//    bf16 over the first source's tile, in the swizzled layout the MMA reads.
+//    It computes in packed bf16 arithmetic (two channels an instruction),
+//    each fp32 weight split as bf16 hi + lo so that no weight is rounded:
+//    four packed FMAs a channel pair instead of seven fp32 operations with
+//    their conversions, at the cost of one rounding of the second source's
+//    partial product.  Its step k fuses V_{k-1} and K_k, the tiles MMA step
+//    k reads, and signals one barrier per step.
 // Every wait is bounded; a wait that runs out sets an abort flag that each
 // role checks, flags the device status, and the CTA frees its tensor memory.
 #include <cfloat>
@@ -49,6 +53,13 @@ constexpr float RESCALE_SLACK = 8.f; // log2 growth of the running max tolerated
 constexpr int NSR = 8;               // fusion-step barriers (more than any ring has slots)
 
 constexpr int cap4(int x) { return x > 4 ? 4 : x; }
+
+__device__ __forceinline__ __nv_bfloat162 bf162_of(uint32_t w) {
+  return *reinterpret_cast<const __nv_bfloat162*>(&w);
+}
+__device__ __forceinline__ uint32_t u32_of(__nv_bfloat162 v) {
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 template <int D>
 struct FwCfg {
@@ -122,7 +133,9 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
   uint8_t* sV = sK + NSK * C::KV_BYTES;
   uint8_t* sK1 = sV + NSV * C::KV_BYTES;               // second source
   uint8_t* sV1 = sK1 + NS1 * C::KV_BYTES;
-  float* sW = reinterpret_cast<float*>(sV1 + NS1 * C::KV_BYTES);   // a0, a1, b0, b1
+  // the fusion weights a0, a1, b0, b1, each as D/2 bf16 pairs split in two:
+  // w = hi + lo, hi = bf16(w), lo = bf16(w - hi) (hi pairs, then lo pairs)
+  uint32_t* sW = reinterpret_cast<uint32_t*>(sV1 + NS1 * C::KV_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sW + 4 * D);
   uint64_t* q_ready = bars;
   uint64_t* k_full = q_ready + 1;   // [4] each ring's barriers, padded to 4
@@ -198,11 +211,14 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
     sm_issued[0] = sm_issued[1] = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < D; i += C::THREADS) {
-    sW[i] = p.a0[kh * D + i];
-    sW[D + i] = p.a1[kh * D + i];
-    sW[2 * D + i] = p.b0[kh * D + i];
-    sW[3 * D + i] = p.b1[kh * D + i];
+  for (int i = tid; i < 2 * D; i += C::THREADS) {   // (vector, channel pair)
+    const int v = i / (D / 2), pc = i % (D / 2);
+    const float* src = v == 0 ? p.a0 : v == 1 ? p.a1 : v == 2 ? p.b0 : p.b1;
+    const float w0 = src[kh * D + 2 * pc], w1 = src[kh * D + 2 * pc + 1];
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(w0, w1);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(w0 - __low2float(hi), w1 - __high2float(hi));
+    sW[v * D + pc] = *reinterpret_cast<const uint32_t*>(&hi);
+    sW[v * D + D / 2 + pc] = *reinterpret_cast<const uint32_t*>(&lo);
   }
   if (warp == C::MMA_WARP) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
@@ -220,7 +236,9 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
     // all of them, so the thread combines one 8-column group per block.
     const int lc = (ft & 3) ^ ((ft >> 3) & 3);
     constexpr int PER_BLOCK = (BN * 4 + 127) / 128;   // 4 (the last one for ft < 64)
-    auto fuse = [&](uint8_t* d0, const uint8_t* d1, const float* w0, const float* w1) {
+    // w0, w1: the split weight pairs of the two sources (hi pairs at [0, D/2),
+    // lo pairs at [D/2, D))
+    auto fuse = [&](uint8_t* d0, const uint8_t* d1, const uint32_t* w0, const uint32_t* w1) {
 #pragma unroll
       for (int cb = 0; cb < CB; ++cb) {
         const int col = cb * SWE + lc * 8;
@@ -235,15 +253,14 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
             ys[i] = *reinterpret_cast<const uint4*>(d1 + (size_t)(cb * BN * 4 + q) * 16);
           }
         }
-        // the block's 8 weights of each source, two 16-byte loads apiece
-        const float4 wa0 = *reinterpret_cast<const float4*>(w0 + col);
-        const float4 wa1 = *reinterpret_cast<const float4*>(w0 + col + 4);
-        const float4 wb0 = *reinterpret_cast<const float4*>(w1 + col);
-        const float4 wb1 = *reinterpret_cast<const float4*>(w1 + col + 4);
-        const float2 u0[4] = {make_float2(wa0.x, wa0.y), make_float2(wa0.z, wa0.w),
-                              make_float2(wa1.x, wa1.y), make_float2(wa1.z, wa1.w)};
-        const float2 u1[4] = {make_float2(wb0.x, wb0.y), make_float2(wb0.z, wb0.w),
-                              make_float2(wb1.x, wb1.y), make_float2(wb1.z, wb1.w)};
+        // the block's 4 weight pairs of each source, hi and lo: 16 bytes apiece
+        const int pc = col / 2;
+        const uint4 h0 = *reinterpret_cast<const uint4*>(w0 + pc);
+        const uint4 l0 = *reinterpret_cast<const uint4*>(w0 + D / 2 + pc);
+        const uint4 h1 = *reinterpret_cast<const uint4*>(w1 + pc);
+        const uint4 l1 = *reinterpret_cast<const uint4*>(w1 + D / 2 + pc);
+        const uint32_t w0h[4] = {h0.x, h0.y, h0.z, h0.w}, w0l[4] = {l0.x, l0.y, l0.z, l0.w};
+        const uint32_t w1h[4] = {h1.x, h1.y, h1.z, h1.w}, w1l[4] = {l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
         for (int i = 0; i < PER_BLOCK; ++i) {
           const int q = ft + 128 * i;
@@ -253,12 +270,16 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
           uint32_t o[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            // w0 * x + w1 * y per channel pair: one packed multiply, one packed FMA
-            const float2 fx = make_float2(bf16lo(xw[e]), bf16hi(xw[e]));
-            const float2 fy = make_float2(bf16lo(yw[e]), bf16hi(yw[e]));
-            const float2 f = __ffma2_rn(u0[e], fx, __fmul2_rn(u1[e], fy));
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(f.x, f.y);
-            o[e] = *reinterpret_cast<uint32_t*>(&v2);
+            // w0 * x + w1 * y per channel pair in packed bf16 arithmetic, with
+            // each weight as hi + lo so that it keeps its fp32 value to 2^-16:
+            // the small lo products first, then the hi products; one rounding
+            // of the w1 * y partial sum and the final one
+            const __nv_bfloat162 x = bf162_of(xw[e]), y = bf162_of(yw[e]);
+            __nv_bfloat162 acc = __hmul2(bf162_of(w0l[e]), x);
+            acc = __hfma2(bf162_of(w1l[e]), y, acc);
+            acc = __hfma2(bf162_of(w1h[e]), y, acc);
+            acc = __hfma2(bf162_of(w0h[e]), x, acc);
+            o[e] = u32_of(acc);
           }
           *reinterpret_cast<uint4*>(d0 + (size_t)(cb * BN * 4 + q) * 16) =
               make_uint4(o[0], o[1], o[2], o[3]);
