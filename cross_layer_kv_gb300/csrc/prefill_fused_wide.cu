@@ -92,7 +92,7 @@ struct FwCfg {
   static constexpr int REGS_FUSION = FKV_PFW_REGS_FUSION;
   static constexpr int REGS_SOFTMAX = FKV_PFW_REGS_SOFTMAX;
 #else
-  static constexpr int REGS_CONTROL = 56, REGS_FUSION = 96, REGS_SOFTMAX = 176;
+  static constexpr int REGS_CONTROL = 56, REGS_FUSION = 80, REGS_SOFTMAX = 184;
 #endif
   static constexpr long long REGS_SPLIT =
       (long long)NG * 128 * REGS_SOFTMAX + 128LL * REGS_CONTROL + 128LL * REGS_FUSION;
