@@ -16,9 +16,11 @@
 //    tiles once and the source tiles of 64 keys into two rings: the first
 //    source's K and V (the fused tiles are written over them) and the
 //    second source's;
-//  * a fusion warpgroup combines the two sources of each K and V tile in
-//    fp32 and writes the bf16 result in place, in the swizzled layout the
-//    tensor cores read (the fused tile serves all G heads);
+//  * a fusion warpgroup combines the two sources of each K and V tile and
+//    writes the bf16 result in place, in the swizzled layout the tensor
+//    cores read (the fused tile serves all G heads); it computes in packed
+//    bf16 arithmetic with each fp32 weight split as bf16 hi + lo (four packed
+//    FMAs a channel pair, lo terms first);
 //  * one MMA warp per head issues tcgen05.mma: S_h = Q_h K^T into a
 //    double-buffered tensor-memory tile, and O_h += P_h V accumulated in
 //    tensor memory; the S of the next tile is issued before the P of this one
@@ -82,6 +84,13 @@ struct PrefillMaps {
 constexpr int SMEM_LIMIT = 232448;   // opt-in dynamic shared memory per CTA (227 KB)
 constexpr int AUX_BYTES = 512;       // barriers, TMEM slot, abort flag
 constexpr float RESCALE_SLACK = 8.f; // log2 growth of the running max tolerated before O is rescaled
+
+__device__ __forceinline__ __nv_bfloat162 bf162_of(uint32_t w) {
+  return *reinterpret_cast<const __nv_bfloat162*>(&w);
+}
+__device__ __forceinline__ uint32_t u32_of(__nv_bfloat162 v) {
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 template <int D, int NSRC, int G>
 struct PrefillPlan {
@@ -151,7 +160,9 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sKV = sQ + G * Cfg::Q_BYTES;
   uint8_t* sB = sKV + NA * PL::SLOT;
-  float* sW = reinterpret_cast<float*>(sB + NB * PL::SLOT);
+  // the fusion weights a0, a1, b0, b1, each as D/2 bf16 pairs split in two:
+  // w = hi + lo, hi = bf16(w), lo = bf16(w - hi) (hi pairs, then lo pairs)
+  uint32_t* sW = reinterpret_cast<uint32_t*>(sB + NB * PL::SLOT);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sW + 4 * D);
   uint64_t* bar_q = bars;
   uint64_t* a_full = bars + 1;          // [NA] first-source tiles landed
@@ -219,11 +230,14 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
     *sm_issued = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < D; i += PL::THREADS) {
-    sW[i] = p.a0[kh * D + i];
-    sW[D + i] = p.a1[kh * D + i];
-    sW[2 * D + i] = p.b0[kh * D + i];
-    sW[3 * D + i] = p.b1[kh * D + i];
+  for (int i = tid; i < 2 * D; i += PL::THREADS) {   // (vector, channel pair)
+    const int v = i / (D / 2), pc = i % (D / 2);
+    const float* src = v == 0 ? p.a0 : v == 1 ? p.a1 : v == 2 ? p.b0 : p.b1;
+    const float w0 = src[kh * D + 2 * pc], w1 = src[kh * D + 2 * pc + 1];
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(w0, w1);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(w0 - __low2float(hi), w1 - __high2float(hi));
+    sW[v * D + pc] = *reinterpret_cast<const uint32_t*>(&hi);
+    sW[v * D + D / 2 + pc] = *reinterpret_cast<const uint32_t*>(&lo);
   }
   if (warp == PL::MMA_WARP) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
@@ -329,8 +343,8 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
         for (int t = 0; t < 2; ++t) {
           uint8_t* d0 = t == 0 ? stage_k(j, 0) : stage_v(j, 0);
           const uint8_t* d1 = t == 0 ? stage_k(j, 1) : stage_v(j, 1);
-          const float* w0 = sW + (t == 0 ? 0 : 2 * D);
-          const float* w1 = sW + (t == 0 ? D : 3 * D);
+          const uint32_t* w0 = sW + (t == 0 ? 0 : 2 * D);
+          const uint32_t* w1 = sW + (t == 0 ? D : 3 * D);
           // all of the thread's chunks of both sources first, so that no
           // load waits behind the stores of an earlier chunk
           constexpr int PER = 2 * CB;
@@ -345,12 +359,14 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
           for (int cb = 0; cb < CB; ++cb) {
             const int col = cb * SWE + lc * 8;
             if (col >= D) continue;  // padding columns stay zero
-            float2 u0[4], u1[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              u0[e] = *reinterpret_cast<const float2*>(w0 + col + 2 * e);
-              u1[e] = *reinterpret_cast<const float2*>(w1 + col + 2 * e);
-            }
+            // the block's 4 weight pairs of each source, hi and lo: 16 bytes apiece
+            const int pc = col / 2;
+            const uint4 h0 = *reinterpret_cast<const uint4*>(w0 + pc);
+            const uint4 l0 = *reinterpret_cast<const uint4*>(w0 + D / 2 + pc);
+            const uint4 h1 = *reinterpret_cast<const uint4*>(w1 + pc);
+            const uint4 l1 = *reinterpret_cast<const uint4*>(w1 + D / 2 + pc);
+            const uint32_t w0h[4] = {h0.x, h0.y, h0.z, h0.w}, w0l[4] = {l0.x, l0.y, l0.z, l0.w};
+            const uint32_t w1h[4] = {h1.x, h1.y, h1.z, h1.w}, w1l[4] = {l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int i = 2 * cb + h;
@@ -359,12 +375,15 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
               uint32_t o[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                // a0 * x + a1 * y per channel pair: one packed multiply, one packed FMA
-                const float2 fx = make_float2(bf16lo(xw[e]), bf16hi(xw[e]));
-                const float2 fy = make_float2(bf16lo(yw[e]), bf16hi(yw[e]));
-                const float2 f = __ffma2_rn(u0[e], fx, __fmul2_rn(u1[e], fy));
-                __nv_bfloat162 v2 = __floats2bfloat162_rn(f.x, f.y);
-                o[e] = *reinterpret_cast<uint32_t*>(&v2);
+                // a0 * x + a1 * y per channel pair in packed bf16 arithmetic,
+                // each weight as hi + lo (lo products first; one rounding of
+                // the a1 * y partial sum and the final one)
+                const __nv_bfloat162 xb = bf162_of(xw[e]), yb = bf162_of(yw[e]);
+                __nv_bfloat162 acc = __hmul2(bf162_of(w0l[e]), xb);
+                acc = __hfma2(bf162_of(w1l[e]), yb, acc);
+                acc = __hfma2(bf162_of(w1h[e]), yb, acc);
+                acc = __hfma2(bf162_of(w0h[e]), xb, acc);
+                o[e] = u32_of(acc);
               }
               *reinterpret_cast<uint4*>(d0 + (size_t)(ft + 128 * i) * 16) =
                   make_uint4(o[0], o[1], o[2], o[3]);
