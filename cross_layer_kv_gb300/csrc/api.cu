@@ -28,6 +28,7 @@ struct fkv_ctx {
   std::vector<int> fused_src[4];           // fused sources: K first, K second, V first, V second
   std::vector<int> window;                 // sliding window per layer (0: full attention)
   std::vector<char> q4;                    // layer cache holds 4-bit records
+  std::vector<int> ring;                   // > 0: the layer's caches are rings of that many rows
 };
 
 namespace {
@@ -114,21 +115,26 @@ fkv_status resolve_sources_impl(const fkv_ctx* c, int layer, int mode, const voi
 }
 
 // Sources and their storage format: *q4 = 1 if every source layer holds
-// 4-bit records, 0 if none does; a mix is FKV_ERR_UNSUPPORTED.
+// 4-bit records, 0 if none does; *ring = the row count of the sources' ring
+// caches, 0 if they are full-length.  A mix of formats or of ring sizes is
+// FKV_ERR_UNSUPPORTED (the sources of a call are read at the same rows).
 fkv_status resolve_sources(const fkv_ctx* c, int layer, int mode, const void* k[2],
                            const void* v[2], const float* a[2], const float* b[2], int* nsrc,
-                           int* q4 = nullptr) {
+                           int* q4, int* ring) {
   int src[4];
   const fkv_status s = resolve_sources_impl(c, layer, mode, k, v, a, b, nsrc, src);
   if (s != FKV_OK) return s;
-  int nq = 0, nt = 0;
+  int nq = 0, nt = 0, r = -1;
   for (int i = 0; i < 4; ++i) {
     if (src[i] <= 0) continue;
     ++nt;
     nq += c->q4[src[i]] ? 1 : 0;
+    if (r >= 0 && c->ring[src[i]] != r) return FKV_ERR_UNSUPPORTED;
+    r = c->ring[src[i]];
   }
   if (nq != 0 && nq != nt) return FKV_ERR_UNSUPPORTED;
-  if (q4) *q4 = nq ? 1 : 0;
+  *q4 = nq ? 1 : 0;
+  *ring = r > 0 ? r : 0;
   return FKV_OK;
 }
 
@@ -160,9 +166,11 @@ fkv_status decode_attn_impl(fkv_ctx* c, const void* q, int layer, int mode,
                             size_t workspace_bytes, void* stream, bool clear_counts) {
   if (!c) return FKV_ERR_INVALID_ARG;
   fkv::DecodeArgs d = decode_args(c);
-  int q4 = 0;
-  fkv_status s = resolve_sources(c, layer, mode, d.k, d.v, d.a, d.b, &d.nsrc, &q4);
+  int q4 = 0, ring = 0;
+  fkv_status s = resolve_sources(c, layer, mode, d.k, d.v, d.a, d.b, &d.nsrc, &q4, &ring);
   if (s != FKV_OK) return s;
+  // ring caches hold the last `ring` positions: the layer must attend within them
+  if (ring > 0 && (c->window[layer] < 1 || c->window[layer] > ring)) return FKV_ERR_INVALID_ARG;
   if (!q || !out || !seq_lens || !aligned16(q) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return FKV_ERR_INVALID_ARG;
@@ -177,6 +185,7 @@ fkv_status decode_attn_impl(fkv_ctx* c, const void* q, int layer, int mode,
   d.seq_lens = seq_lens;
   d.workspace = static_cast<float*>(workspace);
   d.window = c->window[layer];
+  d.ring = ring;
   unsigned ep = g_decode_epoch.fetch_add(1);
   if (ep == 0) ep = g_decode_epoch.fetch_add(1);
   d.epoch = ep;
@@ -211,6 +220,7 @@ fkv_status fkv_create(const fkv_config* cfg, fkv_ctx** out) {
   for (auto& w : c->w) w.assign(cfg->num_layers + 1, nullptr);
   c->window.assign(cfg->num_layers + 1, 0);
   c->q4.assign(cfg->num_layers + 1, 0);
+  c->ring.assign(cfg->num_layers + 1, 0);
   c->lite_src[0].assign(cfg->num_layers + 1, c->n);  // K^n
   c->lite_src[1].assign(cfg->num_layers + 1, 1);     // V^1
   c->fused_src[0].assign(cfg->num_layers + 1, 1);
@@ -307,11 +317,19 @@ fkv_status fkv_set_window(fkv_ctx* c, int layer, int window) {
   return FKV_OK;
 }
 
+fkv_status fkv_set_ring_rows(fkv_ctx* c, int layer, int rows) {
+  if (!c || layer < 1 || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
+  if (rows < 0 || rows > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
+  c->ring[layer] = rows == c->cfg.max_seq ? 0 : rows;
+  return FKV_OK;
+}
+
 fkv_status fkv_append_kv(fkv_ctx* c, int layer, const void* k_new, const void* v_new,
                          const int32_t* pos, int T, void* stream) {
   if (!c || layer < 1 || layer > c->cfg.num_layers) return FKV_ERR_INVALID_ARG;
   if (layer > c->n && !c->cfg.store_upper) return FKV_ERR_UNSUPPORTED;
   if (T < 0 || T > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
+  if (c->ring[layer] > 0 && T > c->ring[layer]) return FKV_ERR_INVALID_ARG;
   if (!c->k[layer] || !c->v[layer]) return FKV_ERR_INVALID_ARG;
   if (T == 0) return FKV_OK;
   if (!k_new || !v_new || !pos || !aligned16(k_new) || !aligned16(v_new) ||
@@ -330,6 +348,7 @@ fkv_status fkv_append_kv(fkv_ctx* c, int layer, const void* k_new, const void* v
   a.head_dim = c->cfg.head_dim;
   a.T = T;
   a.elem_bytes = elem_bytes(c->cfg);
+  a.ring = c->ring[layer];
   const cudaError_t e = c->q4[layer] ? fkv::append_q4_launch(a, static_cast<cudaStream_t>(stream))
                                      : fkv::append_launch(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
@@ -367,12 +386,15 @@ fkv_status fkv_prefill_attn_chunk(fkv_ctx* c, const void* q, int layer, int mode
   if (!c) return FKV_ERR_INVALID_ARG;
   const int S = C;
   fkv::PrefillArgs p{};
-  int q4 = 0;
-  fkv_status s = resolve_sources(c, layer, mode, p.k, p.v, p.a, p.b, &p.nsrc, &q4);
+  int q4 = 0, ring = 0;
+  fkv_status s = resolve_sources(c, layer, mode, p.k, p.v, p.a, p.b, &p.nsrc, &q4, &ring);
   if (s != FKV_OK) return s;
   if (q4) return FKV_ERR_UNSUPPORTED;   // prefill reads bf16 caches
   if (c->cfg.dtype != FKV_BF16) return FKV_ERR_UNSUPPORTED;
   if (S < 1 || q_start < 0 || (long long)q_start + S > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
+  // over ring caches, only while the prompt's positions have not wrapped
+  if (ring > 0 && (long long)q_start + S > ring) return FKV_ERR_UNSUPPORTED;
+  p.plane_rows = ring > 0 ? ring : c->cfg.max_seq;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return FKV_ERR_INVALID_ARG;
   p.q_start = q_start;
   p.window = c->window[layer];

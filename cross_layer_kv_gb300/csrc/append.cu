@@ -29,7 +29,10 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
       continue;
     }
     const size_t src = (((size_t)b * a.kv_heads + h) * a.T + t) * chunks + c;
-    const size_t dst = (((size_t)b * a.kv_heads + h) * a.max_seq + p + t) * chunks + c;
+    // a ring cache keeps position p + t at row (p + t) % ring
+    const int rows = a.ring > 0 ? a.ring : a.max_seq;
+    const int row = a.ring > 0 ? (p + t) % a.ring : p + t;
+    const size_t dst = (((size_t)b * a.kv_heads + h) * rows + row) * chunks + c;
     reinterpret_cast<uint4*>(a.k_cache)[dst] = reinterpret_cast<const uint4*>(a.k_new)[src];
     reinterpret_cast<uint4*>(a.v_cache)[dst] = reinterpret_cast<const uint4*>(a.v_new)[src];
   }
@@ -65,8 +68,11 @@ __global__ void __launch_bounds__(256) append_q4_kernel(AppendArgs a) {
     }
     const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(which ? a.v_new : a.k_new) +
                                ((((size_t)b * a.kv_heads + h) * a.T + t) * a.head_dim + g * kQ4Group);
+    // a ring cache keeps position p + t at row (p + t) % ring
+    const int rows = a.ring > 0 ? a.ring : a.max_seq;
+    const int row = a.ring > 0 ? (p + t) % a.ring : p + t;
     uint8_t* rec = static_cast<uint8_t*>(which ? a.v_cache : a.k_cache) +
-                   (((size_t)b * a.kv_heads + h) * a.max_seq + p + t) * rq;
+                   (((size_t)b * a.kv_heads + h) * rows + row) * rq;
     float x[kQ4Group];
     const uint4 w0 = reinterpret_cast<const uint4*>(src)[0];
     const uint4 w1 = reinterpret_cast<const uint4*>(src)[1];

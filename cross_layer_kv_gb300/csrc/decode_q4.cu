@@ -160,25 +160,40 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
   }
   RowWalker prod = walk;
 
-  uint8_t* ring = smem + (size_t)warp * NS * STAGE;
+  uint8_t* wring = smem + (size_t)warp * NS * STAGE;   // this warp's stages
   uint64_t* wbars = bars + warp * NS;
   const uint64_t policy = l2_policy_evict_first();
-  const size_t row_stride_u = (size_t)p.S_max * ROWB;
+  const size_t row_stride_u = (size_t)(p.ring > 0 ? p.ring : p.S_max) * ROWB;  // bytes per unit
 
   auto issue = [&](int stage, int b, int h, int t, int n) {
     if (lane == 0) {
-      const size_t off = ((size_t)b * H + h) * row_stride_u + (size_t)(first[b] + t) * ROWB;
-      const uint32_t bytes = (uint32_t)n * ROWB;
-      uint8_t* dst = ring + (size_t)stage * STAGE;
+      // rows of positions first[b] + t .. + n - 1; in a ring cache they may
+      // wrap past its end, and then take a second copy from its start
+      const int pos = first[b] + t;
+      const int r0 = p.ring > 0 ? pos % p.ring : pos;
+      const int n1 = p.ring > 0 && r0 + n > p.ring ? p.ring - r0 : n;
+      const size_t base = ((size_t)b * H + h) * row_stride_u;
+      const size_t off = base + (size_t)r0 * ROWB;
+      const uint32_t bytes = (uint32_t)n1 * ROWB;
+      const uint32_t bytes2 = (uint32_t)(n - n1) * ROWB;
+      uint8_t* dst = wring + (size_t)stage * STAGE;
       uint64_t* bar = &wbars[stage];
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, bytes * 2 * NSRC);
-      bulk_g2s(dst, static_cast<const uint8_t*>(p.k0) + off, bytes, bar, policy);
-      if constexpr (NSRC == 2)
-        bulk_g2s(dst + TILE, static_cast<const uint8_t*>(p.k1) + off, bytes, bar, policy);
-      bulk_g2s(dst + NSRC * TILE, static_cast<const uint8_t*>(p.v0) + off, bytes, bar, policy);
-      if constexpr (NSRC == 2)
-        bulk_g2s(dst + 3 * TILE, static_cast<const uint8_t*>(p.v1) + off, bytes, bar, policy);
+      mbar_arrive_expect_tx(bar, (uint32_t)n * ROWB * 2 * NSRC);
+      const void* src[2 * NSRC];
+      src[0] = p.k0;
+      src[NSRC] = p.v0;
+      if constexpr (NSRC == 2) {
+        src[1] = p.k1;
+        src[3] = p.v1;
+      }
+#pragma unroll
+      for (int i = 0; i < 2 * NSRC; ++i) {
+        bulk_g2s(dst + i * TILE, static_cast<const uint8_t*>(src[i]) + off, bytes, bar, policy);
+        if (bytes2)
+          bulk_g2s(dst + i * TILE + bytes, static_cast<const uint8_t*>(src[i]) + base, bytes2, bar,
+                   policy);
+      }
     }
   };
 
@@ -257,7 +272,7 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
       return;
     }
 
-    const uint8_t* st = ring + (size_t)stage * STAGE;
+    const uint8_t* st = wring + (size_t)stage * STAGE;
 
     // scores
     float s[STEPS][G];
@@ -458,6 +473,7 @@ cudaError_t launch_q4(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t 
   sp.H_kv = a.kv_heads;
   sp.S_max = a.max_seq;
   sp.window = a.window;
+  sp.ring = a.ring;
   sp.qscale = a.softmax_scale * 1.4426950408889634f;
   auto kern = decode_q4_kernel<D, NSRC, WGT || NSRC == 2, G>;
   cudaError_t e =

@@ -34,6 +34,8 @@ struct DecodeArgs {
   float softmax_scale;
   int num_ctas;              // split grid (0 = library default)
   int window;                // > 0: attend only to the last `window` rows
+  int ring;                  // > 0: the source caches are rings of this many rows per
+                             // unit (position t at row t % ring); 0: S_max rows, row = position
   unsigned epoch;            // distinct per call (tags the unit arrival counts)
 };
 
@@ -80,6 +82,7 @@ struct AppendArgs {
   const int32_t* pos;
   int* status;
   int batch, kv_heads, max_seq, head_dim, T, elem_bytes;
+  int ring;        // > 0: the cache is a ring of this many rows per unit (row = position % ring)
 };
 
 cudaError_t append_launch(const AppendArgs& a, cudaStream_t stream);
@@ -108,6 +111,8 @@ struct PrefillArgs {
   int batch, kv_heads, group, max_seq, head_dim, S;
   int q_start;     // cache position of query row 0 (0 for a whole prompt)
   int window;      // > 0: sliding window of that many positions
+  int plane_rows;  // cache rows per (b, kv-head) unit (S_max, or a ring's rows; positions
+                   // [0, q_start + S) must map to rows unchanged)
   int nsrc;
   float softmax_scale;
 };

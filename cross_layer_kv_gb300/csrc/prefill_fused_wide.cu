@@ -598,7 +598,7 @@ cudaError_t launch_fused_wide(const PrefillArgs& a, cudaStream_t stream) {
   FwMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const long long units = (long long)a.batch * a.kv_heads;
-  const size_t kv_plane = (size_t)a.max_seq * D * 2;
+  const size_t kv_plane = (size_t)a.plane_rows * D * 2;   // bytes per (b, kv-head) plane
   const int S_kv = a.q_start + a.S;
   bool ok = make_map(&maps.k0, a.k[0], D, S_kv, units, kv_plane, BN);
   ok = ok && make_map(&maps.k1, a.k[1], D, S_kv, units, kv_plane, BN);

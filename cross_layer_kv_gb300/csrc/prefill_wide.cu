@@ -468,7 +468,7 @@ cudaError_t launch_wide(const PrefillArgs& a, cudaStream_t stream) {
   WideMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const long long units = (long long)a.batch * a.kv_heads;
-  const size_t kv_plane = (size_t)a.max_seq * D * 2;
+  const size_t kv_plane = (size_t)a.plane_rows * D * 2;   // bytes per (b, kv-head) plane
   const int S_kv = a.q_start + a.S;
   bool ok = make_map(&maps.q, a.q, D, a.S, (long long)a.batch * a.kv_heads * a.group,
                      (size_t)a.S * D * 2, BM);

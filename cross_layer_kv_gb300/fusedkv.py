@@ -71,6 +71,7 @@ _SIGS = {
     "fkv_set_sources": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int]),
     "fkv_set_window": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int]),
+    "fkv_set_ring_rows": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int]),
     "fkv_append_kv": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, ctypes.c_int, _P]),
     "fkv_decode_workspace_bytes": (ctypes.c_size_t, [_P]),
     "fkv_decode_attn": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, _P, _P, _P,
@@ -158,6 +159,7 @@ class Context:
         _check(self._lib.fkv_create(ctypes.byref(self.cfg), ctypes.byref(h)), "fkv_create")
         self.handle = h
         self._keep = {}
+        self._ring = {}   # layer -> ring rows (layers with full-length caches absent)
 
     # -- lifetime --------------------------------------------------------
     def close(self):
@@ -179,9 +181,13 @@ class Context:
         self.close()
 
     # -- shape checks (marshalling only) ---------------------------------
-    def _cache_shape(self):
+    def _rows(self, layer: int) -> int:
+        """Cache rows per (batch row, KV head) of a layer: S_max, or its ring's rows."""
+        return self._ring.get(layer) or self.cfg.max_seq
+
+    def _cache_shape(self, layer: int):
         c = self.cfg
-        return (c.batch, c.num_kv_heads, c.max_seq, c.head_dim)
+        return (c.batch, c.num_kv_heads, self._rows(layer), c.head_dim)
 
     def _need(self, t: torch.Tensor, shape, dtype, name):
         if not isinstance(t, torch.Tensor):
@@ -192,8 +198,8 @@ class Context:
 
     # -- the C calls -----------------------------------------------------
     def fkv_bind_layer_cache(self, layer: int, k, v):
-        self._need(k, self._cache_shape(), self.torch_dtype, "k cache")
-        self._need(v, self._cache_shape(), self.torch_dtype, "v cache")
+        self._need(k, self._cache_shape(layer), self.torch_dtype, "k cache")
+        self._need(v, self._cache_shape(layer), self.torch_dtype, "v cache")
         _check(self._lib.fkv_bind_layer_cache(self.handle, layer, _ptr(k), _ptr(v)),
                "fkv_bind_layer_cache")
         self._keep[("kv", layer)] = (k, v)
@@ -201,15 +207,15 @@ class Context:
     def fkv_q4_row_bytes(self) -> int:
         return int(self._lib.fkv_q4_row_bytes(self.cfg.head_dim))
 
-    def q4_cache(self, device="cuda") -> torch.Tensor:
-        """A zeroed uint8 [B, H_kv, S_max, fkv_q4_row_bytes(D)] buffer."""
+    def q4_cache(self, device="cuda", rows: Optional[int] = None) -> torch.Tensor:
+        """A zeroed uint8 [B, H_kv, rows (default S_max), fkv_q4_row_bytes(D)] buffer."""
         c = self.cfg
-        return torch.zeros((c.batch, c.num_kv_heads, c.max_seq, self.fkv_q4_row_bytes()),
+        return torch.zeros((c.batch, c.num_kv_heads, rows or c.max_seq, self.fkv_q4_row_bytes()),
                            dtype=torch.uint8, device=device)
 
     def fkv_bind_layer_cache_q4(self, layer: int, k_rec, v_rec):
         c = self.cfg
-        shape = (c.batch, c.num_kv_heads, c.max_seq, self.fkv_q4_row_bytes())
+        shape = (c.batch, c.num_kv_heads, self._rows(layer), self.fkv_q4_row_bytes())
         self._need(k_rec, shape, torch.uint8, "k records")
         self._need(v_rec, shape, torch.uint8, "v records")
         _check(self._lib.fkv_bind_layer_cache_q4(self.handle, layer, _ptr(k_rec), _ptr(v_rec)),
@@ -234,6 +240,15 @@ class Context:
 
     def fkv_set_window(self, layer: int, window: int):
         _check(self._lib.fkv_set_window(self.handle, layer, window), "fkv_set_window")
+
+    def fkv_set_ring_rows(self, layer: int, rows: int):
+        """Make a layer's caches rings of `rows` rows (0: full length).  Bind
+        the layer's caches after this call: the bind checks their row count."""
+        _check(self._lib.fkv_set_ring_rows(self.handle, layer, rows), "fkv_set_ring_rows")
+        if rows in (0, self.cfg.max_seq):
+            self._ring.pop(layer, None)
+        else:
+            self._ring[layer] = rows
 
     def fkv_append_kv(self, layer: int, k_new, v_new, pos, T: Optional[int] = None, stream=None):
         c = self.cfg

@@ -156,6 +156,27 @@ fkv_status fkv_set_sources(fkv_ctx* ctx, int layer, int mode, int k_first, int k
  * negative window. */
 fkv_status fkv_set_window(fkv_ctx* ctx, int layer, int window);
 
+/* Make the caches of `layer` rings of `rows` rows per (batch row, KV head):
+ * position t of a sequence lives at row t % rows, so a sliding-window layer
+ * stores only the positions its window can reach instead of S_max rows (the
+ * capacity half of the hybrid sliding-window sharing of the FusedKV slides,
+ * "MoE and hybrid SWA").  The buffers bound to the layer (fkv_bind_layer_cache
+ * or fkv_bind_layer_cache_q4, before or after this call) are then
+ * [B, H_kv, rows, D] (or rows records).  rows = 0 (or S_max) restores the
+ * full-length layout; FKV_ERR_INVALID_ARG for a bad layer or rows outside
+ * [0, S_max].
+ * Calls over ring caches:
+ *   - fkv_append_kv writes position pos[b] + i at row (pos[b] + i) % rows;
+ *     T <= rows (FKV_ERR_INVALID_ARG otherwise); rows of positions older than
+ *     the last `rows` are overwritten, so append every position in order;
+ *   - fkv_decode_attn needs every source of the call to be a ring of the same
+ *     size (FKV_ERR_UNSUPPORTED otherwise) and the attending layer to have a
+ *     window with 1 <= window <= rows (FKV_ERR_INVALID_ARG otherwise); a tile
+ *     of rows that wraps past the ring's end is read in two copies;
+ *   - fkv_prefill_attn / _chunk run only while the call's positions have not
+ *     wrapped, q_start + C <= rows (FKV_ERR_UNSUPPORTED otherwise). */
+fkv_status fkv_set_ring_rows(fkv_ctx* ctx, int layer, int rows);
+
 /* Write the post-RoPE K/V of T new tokens into a layer's cache (the storage
  * caches take the new token before the upper layers attend; reading notes
  * §2.3).  k_new, v_new: device [B, H_kv, T, D] in the context dtype.
