@@ -108,7 +108,9 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
     }
     const int Le = p.window > 0 && L > p.window ? p.window : L;
     lens[i] = Le;
-    first[i] = L - Le;
+    // cache row of the first attended position (in a ring: its row, so that
+    // the copies below need no division)
+    first[i] = p.ring > 0 ? (L - Le) % p.ring : L - Le;
   }
   __syncthreads();
   if (warp == 0) {
@@ -167,32 +169,42 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
 
   auto issue = [&](int stage, int b, int h, int t, int n) {
     if (lane == 0) {
-      // rows of positions first[b] + t .. + n - 1; in a ring cache they may
-      // wrap past its end, and then take a second copy from its start
-      const int pos = first[b] + t;
-      const int r0 = p.ring > 0 ? pos % p.ring : pos;
-      const int n1 = p.ring > 0 && r0 + n > p.ring ? p.ring - r0 : n;
-      const size_t base = ((size_t)b * H + h) * row_stride_u;
-      const size_t off = base + (size_t)r0 * ROWB;
-      const uint32_t bytes = (uint32_t)n1 * ROWB;
-      const uint32_t bytes2 = (uint32_t)(n - n1) * ROWB;
       uint8_t* dst = wring + (size_t)stage * STAGE;
       uint64_t* bar = &wbars[stage];
+      const size_t base = ((size_t)b * H + h) * row_stride_u;
+      const uint32_t bytes = (uint32_t)n * ROWB;
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, (uint32_t)n * ROWB * 2 * NSRC);
-      const void* src[2 * NSRC];
-      src[0] = p.k0;
-      src[NSRC] = p.v0;
-      if constexpr (NSRC == 2) {
-        src[1] = p.k1;
-        src[3] = p.v1;
-      }
+      mbar_arrive_expect_tx(bar, bytes * 2 * NSRC);
+      if (p.ring == 0) {
+        // rows first + t .. + n - 1 of the unit's plane
+        const size_t off = base + (size_t)(first[b] + t) * ROWB;
+        bulk_g2s(dst, static_cast<const uint8_t*>(p.k0) + off, bytes, bar, policy);
+        if constexpr (NSRC == 2)
+          bulk_g2s(dst + TILE, static_cast<const uint8_t*>(p.k1) + off, bytes, bar, policy);
+        bulk_g2s(dst + NSRC * TILE, static_cast<const uint8_t*>(p.v0) + off, bytes, bar, policy);
+        if constexpr (NSRC == 2)
+          bulk_g2s(dst + 3 * TILE, static_cast<const uint8_t*>(p.v1) + off, bytes, bar, policy);
+      } else {
+        // a ring cache: the rows may wrap past its end (t < window <= ring,
+        // so at most once), and then take a second copy from its start
+        int r0 = first[b] + t;
+        if (r0 >= p.ring) r0 -= p.ring;
+        const int n1 = r0 + n > p.ring ? p.ring - r0 : n;
+        const size_t off = base + (size_t)r0 * ROWB;
+        const uint32_t b1 = (uint32_t)n1 * ROWB, b2 = bytes - b1;
+        const void* src[2 * NSRC];
+        src[0] = p.k0;
+        src[NSRC] = p.v0;
+        if constexpr (NSRC == 2) {
+          src[1] = p.k1;
+          src[3] = p.v1;
+        }
 #pragma unroll
-      for (int i = 0; i < 2 * NSRC; ++i) {
-        bulk_g2s(dst + i * TILE, static_cast<const uint8_t*>(src[i]) + off, bytes, bar, policy);
-        if (bytes2)
-          bulk_g2s(dst + i * TILE + bytes, static_cast<const uint8_t*>(src[i]) + base, bytes2, bar,
-                   policy);
+        for (int i = 0; i < 2 * NSRC; ++i) {
+          bulk_g2s(dst + i * TILE, static_cast<const uint8_t*>(src[i]) + off, b1, bar, policy);
+          if (b2)
+            bulk_g2s(dst + i * TILE + b1, static_cast<const uint8_t*>(src[i]) + base, b2, bar, policy);
+        }
       }
     }
   };
