@@ -392,9 +392,17 @@ fkv_status fkv_prefill_attn_chunk(fkv_ctx* c, const void* q, int layer, int mode
   if (q4) return FKV_ERR_UNSUPPORTED;   // prefill reads bf16 caches
   if (c->cfg.dtype != FKV_BF16) return FKV_ERR_UNSUPPORTED;
   if (S < 1 || q_start < 0 || (long long)q_start + S > c->cfg.max_seq) return FKV_ERR_INVALID_ARG;
-  // over ring caches, only while the prompt's positions have not wrapped
-  if (ring > 0 && (long long)q_start + S > ring) return FKV_ERR_UNSUPPORTED;
+  // Over ring caches whose positions have wrapped, every key a query of the
+  // chunk attends must still be in the ring: a sliding window W with
+  // C + W - 1 <= rows (the kernels also want rows to be a multiple of their
+  // key tile, else FKV_ERR_UNSUPPORTED).
+  if (ring > 0 && (long long)q_start + S > ring) {
+    const int W = c->window[layer];
+    if (W < 1 || W > ring) return FKV_ERR_INVALID_ARG;
+    if ((long long)S + W - 1 > ring) return FKV_ERR_UNSUPPORTED;
+  }
   p.plane_rows = ring > 0 ? ring : c->cfg.max_seq;
+  p.ring = ring;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return FKV_ERR_INVALID_ARG;
   p.q_start = q_start;
   p.window = c->window[layer];

@@ -111,8 +111,9 @@ struct PrefillArgs {
   int batch, kv_heads, group, max_seq, head_dim, S;
   int q_start;     // cache position of query row 0 (0 for a whole prompt)
   int window;      // > 0: sliding window of that many positions
-  int plane_rows;  // cache rows per (b, kv-head) unit (S_max, or a ring's rows; positions
-                   // [0, q_start + S) must map to rows unchanged)
+  int plane_rows;  // cache rows per (b, kv-head) unit (S_max, or a ring's rows)
+  int ring;        // > 0: the caches are rings of that many rows (position t at row
+                   // t % ring), a multiple of the kernel's key tile once positions wrap
   int nsrc;
   float softmax_scale;
 };

@@ -74,6 +74,7 @@ struct PrefillParams {
   int S_kv;     // key rows attended: q_start + C
   int window;   // > 0: a query at position m sees only keys t > m - window
   float scale_log2;
+  int ring;     // > 0: K/V rows are rings of that many rows (a multiple of BN)
 };
 
 struct PrefillMaps {
@@ -260,18 +261,20 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
       int issued = 0;   // copies issued: 2 per tile (ring A, then ring B)
       for (int j = 0; j < ntiles; ++j) {
         const int n0 = (j0 + j) * BN;
+        // the tile's first cache row: in a ring, whole tiles never wrap
+        const int ky = p.ring > 0 ? n0 % p.ring : n0;
         if (j >= NA && !wait(&a_empty[j % NA], (uint32_t)(j / NA - 1) & 1u)) break;
         mbar_arrive_expect_tx(&a_full[j % NA], PL::SLOT);
         for (int cb = 0; cb < CB; ++cb) {
-          tma_load_3d(stage_k(j, 0) + cb * BN * SW, &maps.k0, cb * SWE, n0, unit, &a_full[j % NA]);
-          tma_load_3d(stage_v(j, 0) + cb * BN * SW, &maps.v0, cb * SWE, n0, unit, &a_full[j % NA]);
+          tma_load_3d(stage_k(j, 0) + cb * BN * SW, &maps.k0, cb * SWE, ky, unit, &a_full[j % NA]);
+          tma_load_3d(stage_v(j, 0) + cb * BN * SW, &maps.v0, cb * SWE, ky, unit, &a_full[j % NA]);
         }
         issued = 2 * j + 1;
         if (j >= NB && !wait(&b_empty[j % NB], (uint32_t)(j / NB - 1) & 1u)) break;
         mbar_arrive_expect_tx(&b_full[j % NB], PL::SLOT);
         for (int cb = 0; cb < CB; ++cb) {
-          tma_load_3d(stage_k(j, 1) + cb * BN * SW, &maps.k1, cb * SWE, n0, unit, &b_full[j % NB]);
-          tma_load_3d(stage_v(j, 1) + cb * BN * SW, &maps.v1, cb * SWE, n0, unit, &b_full[j % NB]);
+          tma_load_3d(stage_k(j, 1) + cb * BN * SW, &maps.k1, cb * SWE, ky, unit, &b_full[j % NB]);
+          tma_load_3d(stage_v(j, 1) + cb * BN * SW, &maps.v1, cb * SWE, ky, unit, &b_full[j % NB]);
         }
         issued = 2 * j + 2;
       }
@@ -554,12 +557,18 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   const long long units = (long long)a.batch * a.kv_heads;
   const size_t kv_plane = (size_t)a.plane_rows * D * 2;   // bytes per (b, kv-head) plane
   const int S_kv = a.q_start + a.S;
+  // a ring whose positions have wrapped is read whole (rows past the key
+  // extent hold older positions, masked); otherwise rows from S_kv on read 0.
+  // Whole key tiles map to whole ring rows only if the ring is a multiple of BN.
+  const bool wrapped = a.ring > 0 && S_kv > a.ring;
+  if (wrapped && a.ring % BN != 0) return cudaErrorNotSupported;
+  const int map_rows = wrapped ? a.ring : S_kv;
   bool ok = make_map(&maps.q, a.q, D, a.S, (long long)a.batch * a.kv_heads * G,
                      (size_t)a.S * D * 2, BM);
-  ok = ok && make_map(&maps.k0, a.k[0], D, S_kv, units, kv_plane, BN);
-  ok = ok && make_map(&maps.v0, a.v[0], D, S_kv, units, kv_plane, BN);
-  ok = ok && make_map(&maps.k1, a.k[1], D, S_kv, units, kv_plane, BN);
-  ok = ok && make_map(&maps.v1, a.v[1], D, S_kv, units, kv_plane, BN);
+  ok = ok && make_map(&maps.k0, a.k[0], D, map_rows, units, kv_plane, BN);
+  ok = ok && make_map(&maps.v0, a.v[0], D, map_rows, units, kv_plane, BN);
+  ok = ok && make_map(&maps.k1, a.k[1], D, map_rows, units, kv_plane, BN);
+  ok = ok && make_map(&maps.v1, a.v[1], D, map_rows, units, kv_plane, BN);
   if (!ok) return cudaErrorInvalidValue;
   PrefillParams p;
   p.a0 = a.a[0];
@@ -575,6 +584,7 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   p.q_start = a.q_start;
   p.S_kv = S_kv;
   p.window = a.window;
+  p.ring = a.ring;
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
   const size_t smem = prefill_smem_bytes<D, NSRC, G>();
   auto kern = prefill_kernel<D, NSRC, G>;

@@ -114,6 +114,7 @@ struct FwParams {
   int S_kv;     // key rows attended: q_start + C
   int window;   // > 0: a query at position m sees only keys t > m - window
   float scale_log2;
+  int ring;     // > 0: K/V rows are rings of that many rows (a multiple of BN)
 };
 
 struct FwMaps {
@@ -324,17 +325,19 @@ __global__ void __launch_bounds__(FwCfg<D>::THREADS, 1)
       int issued = 0;   // copies issued: 2 per tile (first source, then second)
       for (int j = 0; j < n_max; ++j) {
         const int n0 = (j0 + j) * BN;
+        // the tile's first cache row: in a ring, whole tiles never wrap
+        const int ky = p.ring > 0 ? n0 % p.ring : n0;
         if (j >= n0s && !wait(&e0[j % n0s], (uint32_t)(j / n0s - 1) & 1u)) break;
         uint8_t* d0 = is_k ? tile_k(j) : tile_v(j);
         mbar_arrive_expect_tx(&f0[j % n0s], C::KV_BYTES);
         for (int cb = 0; cb < CB; ++cb)
-          tma_load_3d(d0 + cb * BN * SW, m0, cb * SWE, n0, unit, &f0[j % n0s]);
+          tma_load_3d(d0 + cb * BN * SW, m0, cb * SWE, ky, unit, &f0[j % n0s]);
         issued = 2 * j + 1;
         if (j >= NS1 && !wait(&e1[j % NS1], (uint32_t)(j / NS1 - 1) & 1u)) break;
         uint8_t* d1 = is_k ? tile_k1(j) : tile_v1(j);
         mbar_arrive_expect_tx(&f1[j % NS1], C::KV_BYTES);
         for (int cb = 0; cb < CB; ++cb)
-          tma_load_3d(d1 + cb * BN * SW, m1, cb * SWE, n0, unit, &f1[j % NS1]);
+          tma_load_3d(d1 + cb * BN * SW, m1, cb * SWE, ky, unit, &f1[j % NS1]);
         issued = 2 * j + 2;
       }
       sm_issued[is_k ? 0 : 1] = issued;
@@ -600,10 +603,16 @@ cudaError_t launch_fused_wide(const PrefillArgs& a, cudaStream_t stream) {
   const long long units = (long long)a.batch * a.kv_heads;
   const size_t kv_plane = (size_t)a.plane_rows * D * 2;   // bytes per (b, kv-head) plane
   const int S_kv = a.q_start + a.S;
-  bool ok = make_map(&maps.k0, a.k[0], D, S_kv, units, kv_plane, BN);
-  ok = ok && make_map(&maps.k1, a.k[1], D, S_kv, units, kv_plane, BN);
-  ok = ok && make_map(&maps.v0, a.v[0], D, S_kv, units, kv_plane, BN);
-  ok = ok && make_map(&maps.v1, a.v[1], D, S_kv, units, kv_plane, BN);
+  // a ring whose positions have wrapped is read whole (rows past the key
+  // extent hold older positions, masked); otherwise rows from S_kv on read 0.
+  // Whole key tiles map to whole ring rows only if the ring is a multiple of BN.
+  const bool wrapped = a.ring > 0 && S_kv > a.ring;
+  if (wrapped && a.ring % BN != 0) return cudaErrorNotSupported;
+  const int map_rows = wrapped ? a.ring : S_kv;
+  bool ok = make_map(&maps.k0, a.k[0], D, map_rows, units, kv_plane, BN);
+  ok = ok && make_map(&maps.k1, a.k[1], D, map_rows, units, kv_plane, BN);
+  ok = ok && make_map(&maps.v0, a.v[0], D, map_rows, units, kv_plane, BN);
+  ok = ok && make_map(&maps.v1, a.v[1], D, map_rows, units, kv_plane, BN);
   if (!ok) return cudaErrorInvalidValue;
   FwParams p;
   p.a0 = a.a[0];
@@ -620,6 +629,7 @@ cudaError_t launch_fused_wide(const PrefillArgs& a, cudaStream_t stream) {
   p.q_start = a.q_start;
   p.S_kv = S_kv;
   p.window = a.window;
+  p.ring = a.ring;
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
   auto kern = prefill_fused_wide_kernel<D>;
   cudaError_t e =

@@ -91,6 +91,7 @@ struct WideParams {
   int S_kv;     // key rows attended: q_start + C
   int window;   // > 0: a query at position m sees only keys t > m - window
   float scale_log2;
+  int ring;     // > 0: K/V rows are rings of that many rows (a multiple of BN)
 };
 
 struct WideMaps {
@@ -197,10 +198,12 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
         const int s = j % NS, u = j / NS;
         if (u > 0 && !wait(&kv_empty[s], (uint32_t)(u - 1) & 1u)) break;
         const int n0 = (j0 + j) * BN;
+        // the tile's first cache row: in a ring, whole tiles never wrap
+        const int ky = p.ring > 0 ? n0 % p.ring : n0;
         mbar_arrive_expect_tx(&kv_full[s], C::STAGE);
         for (int cb = 0; cb < CB; ++cb) {
-          tma_load_3d(stage_k(s) + cb * BN * SW, &maps.k, cb * SWE, n0, unit, &kv_full[s]);
-          tma_load_3d(stage_v(s) + cb * BN * SW, &maps.v, cb * SWE, n0, unit, &kv_full[s]);
+          tma_load_3d(stage_k(s) + cb * BN * SW, &maps.k, cb * SWE, ky, unit, &kv_full[s]);
+          tma_load_3d(stage_v(s) + cb * BN * SW, &maps.v, cb * SWE, ky, unit, &kv_full[s]);
         }
         issued = j + 1;
       }
@@ -470,10 +473,16 @@ cudaError_t launch_wide(const PrefillArgs& a, cudaStream_t stream) {
   const long long units = (long long)a.batch * a.kv_heads;
   const size_t kv_plane = (size_t)a.plane_rows * D * 2;   // bytes per (b, kv-head) plane
   const int S_kv = a.q_start + a.S;
+  // a ring whose positions have wrapped is read whole (rows past the key
+  // extent hold older positions, masked); otherwise rows from S_kv on read 0.
+  // Whole key tiles map to whole ring rows only if the ring is a multiple of BN.
+  const bool wrapped = a.ring > 0 && S_kv > a.ring;
+  if (wrapped && a.ring % BN != 0) return cudaErrorNotSupported;
+  const int map_rows = wrapped ? a.ring : S_kv;
   bool ok = make_map(&maps.q, a.q, D, a.S, (long long)a.batch * a.kv_heads * a.group,
                      (size_t)a.S * D * 2, BM);
-  ok = ok && make_map(&maps.k, a.k[0], D, S_kv, units, kv_plane, BN);
-  ok = ok && make_map(&maps.v, a.v[0], D, S_kv, units, kv_plane, BN);
+  ok = ok && make_map(&maps.k, a.k[0], D, map_rows, units, kv_plane, BN);
+  ok = ok && make_map(&maps.v, a.v[0], D, map_rows, units, kv_plane, BN);
   if (!ok) return cudaErrorInvalidValue;
   WideParams p;
   p.a = a.a[0];
@@ -487,6 +496,7 @@ cudaError_t launch_wide(const PrefillArgs& a, cudaStream_t stream) {
   p.q_start = a.q_start;
   p.S_kv = S_kv;
   p.window = a.window;
+  p.ring = a.ring;
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
   auto kern = prefill_wide_kernel<D>;
   cudaError_t e =

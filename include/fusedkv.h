@@ -173,8 +173,14 @@ fkv_status fkv_set_window(fkv_ctx* ctx, int layer, int window);
  *     size (FKV_ERR_UNSUPPORTED otherwise) and the attending layer to have a
  *     window with 1 <= window <= rows (FKV_ERR_INVALID_ARG otherwise); a tile
  *     of rows that wraps past the ring's end is read in two copies;
- *   - fkv_prefill_attn / _chunk run only while the call's positions have not
- *     wrapped, q_start + C <= rows (FKV_ERR_UNSUPPORTED otherwise). */
+ *   - fkv_prefill_attn / _chunk read rows as they are while the call's
+ *     positions have not wrapped (q_start + C <= rows).  Past that, the layer
+ *     needs a window 1 <= W <= rows (FKV_ERR_INVALID_ARG otherwise), the chunk
+ *     C + W - 1 <= rows, and rows a multiple of the kernel's key tile: 128
+ *     for one source, 112 for fused layers with head_dim <= 96, 64 for fused
+ *     layers with head_dim 128 (FKV_ERR_UNSUPPORTED otherwise; 896 suits all
+ *     three).  Every row must then have been written once, since rows past
+ *     the chunk's last position are read and masked. */
 fkv_status fkv_set_ring_rows(fkv_ctx* ctx, int layer, int rows);
 
 /* Write the post-RoPE K/V of T new tokens into a layer's cache (the storage

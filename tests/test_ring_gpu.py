@@ -221,7 +221,8 @@ def test_ring_q4_decode():
 
 def test_ring_prefill_before_wrap_and_rejections():
     """Prefill over ring caches while the prompt's positions have not wrapped;
-    beyond that, and for inconsistent set-ups, the call is refused."""
+    rings the kernels cannot tile past that, and inconsistent set-ups, are
+    refused."""
     w = _w(96, S=600, Bt=2)
     R, S = 320, 300
     n, layer = w.n, 5
@@ -245,7 +246,8 @@ def test_ring_prefill_before_wrap_and_rejections():
     ref = O.prefill_attn(f64(q), layer, w.num_layers, "fused", kc, vc,
                          weights={layer: tuple(f64(x) for x in wts)}, window=100)
     assert_close(f64(out), ref, "bf16", "prefill over a ring before it wraps")
-    # a chunk past the ring's rows would read wrapped positions
+    # past the ring's rows, a ring that is not a whole number of key tiles
+    # (320 rows against the fused kernel's 112-key tiles) is refused
     qc = q[:, :, :40].contiguous()
     with pytest.raises(B.FkvError) as e:
         ctx.fkv_prefill_attn_chunk(qc, layer, "fused", R - 20, 40, torch.empty_like(qc))
@@ -271,4 +273,67 @@ def test_ring_prefill_before_wrap_and_rejections():
         with pytest.raises(B.FkvError) as e:
             ctx.fkv_set_ring_rows(1, bad)
         assert e.value.status == B.FKV_ERR_INVALID_ARG
+    ctx.close()
+
+
+# (mode, D, G): the one-source kernel (128-key tiles), the fused kernel for
+# D <= 96 (112-key tiles) and the fused D = 128 kernel (64-key tiles)
+_WRAP_CASES = [("lite", 64, 2), ("vanilla", 80, 1), ("fused", 96, 2), ("fused", 128, 1),
+               ("scaled", 128, 2)]
+
+
+@pytest.mark.parametrize("mode,D,G", _WRAP_CASES)
+def test_ring_chunked_prefill_wraps(mode, D, G):
+    """A prompt streamed in chunks through rings of 896 rows (a whole number
+    of every kernel's key tiles): each chunk's K/V appended, then the chunk's
+    causal windowed attention, against the oracle over full-length caches.
+    The chunks cross the ring's end, start on and off the tile grid, and the
+    longest one meets C + W - 1 = R exactly."""
+    R, W = 896, 300
+    chunks = [(0, 500), (500, 597), (1097, 333), (1430, 470), (1900, 401)]
+    S_all = chunks[-1][0] + chunks[-1][1]
+    w = _w(D, G=G, S=S_all, Bt=2)
+    n, layer = w.n, 5
+    need = [layer] if mode == "vanilla" else sorted({1, n})
+    ctx = B.Context(w.num_layers, w.batch, w.seq, w.q_heads, w.kv_heads, w.head_dim, "bf16",
+                    store_upper=(mode == "vanilla"))
+    full, rings = {}, {}
+    for l in need:
+        k, v = synth.make_cache(w, l, 60 + D, "cuda")
+        full[l] = (k, v)
+        ctx.fkv_set_ring_rows(l, R)
+        kr = torch.zeros(w.batch, w.kv_heads, R, D, dtype=torch.bfloat16, device="cuda")
+        rings[l] = (kr, torch.zeros_like(kr))
+        ctx.fkv_bind_layer_cache(l, *rings[l])
+    wts = synth.make_weights(w, layer, 60 + D, "cuda")
+    ctx.fkv_set_fusion_weights(layer, *wts)
+    ctx.fkv_set_window(layer, W)
+    g = torch.Generator(device="cuda").manual_seed(61 + D)
+    q = torch.randn(w.batch, w.q_heads, S_all, D, generator=g, device="cuda").to(torch.bfloat16)
+    ws = {layer: tuple(f64(x) for x in wts)}
+    for q0, C in chunks:
+        pos = torch.full((w.batch,), q0, dtype=torch.int32, device="cuda")
+        for l in need:
+            k, v = full[l]
+            ctx.fkv_append_kv(l, k[:, :, q0:q0 + C].contiguous(), v[:, :, q0:q0 + C].contiguous(),
+                              pos)
+        qc = q[:, :, q0:q0 + C].contiguous()
+        oc = torch.empty_like(qc)
+        ctx.fkv_prefill_attn_chunk(qc, layer, mode, q0, C, oc)
+        assert ctx.fkv_get_device_status() == B.FKV_OK
+        kc = {l: f64(k[:, :, :q0 + C]) for l, (k, v) in full.items()}
+        vc = {l: f64(v[:, :, :q0 + C]) for l, (k, v) in full.items()}
+        ref = O.chunk_prefill_attn(f64(qc), q0, layer, w.num_layers, mode, kc, vc,
+                                   weights=ws, window=W)
+        assert_close(f64(oc), ref, "bf16", "%s D=%d G=%d chunk %d+%d" % (mode, D, G, q0, C))
+    # once wrapped: a chunk too long for its window, and no window, are refused
+    qc = q[:, :, :W].contiguous()
+    ctx.fkv_set_window(layer, R - W + 2)
+    with pytest.raises(B.FkvError) as e:
+        ctx.fkv_prefill_attn_chunk(qc, layer, mode, S_all - W, W, torch.empty_like(qc))
+    assert e.value.status == B.FKV_ERR_UNSUPPORTED
+    ctx.fkv_set_window(layer, 0)
+    with pytest.raises(B.FkvError) as e:
+        ctx.fkv_prefill_attn_chunk(qc, layer, mode, S_all - W, W, torch.empty_like(qc))
+    assert e.value.status == B.FKV_ERR_INVALID_ARG
     ctx.close()
