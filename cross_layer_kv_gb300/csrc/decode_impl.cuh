@@ -543,7 +543,8 @@ __global__ void __launch_bounds__(W * 32, 1) decode_split_kernel(const SplitPara
       fresh = false;
     }
 
-    if (!mbar_wait_bounded(&wbars[stage], parity, wlim)) {
+    // warp-uniform: every lane leaves, or none does (shuffles follow)
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wbars[stage], parity, wlim))) {
       flag_status(p.status, kDevTimeout);
       // Let the copies still in flight land before the CTA can exit: every
       // stage issued and not yet consumed, the one just awaited included.

@@ -276,7 +276,8 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
       fresh = false;
     }
 
-    if (!mbar_wait_bounded(&wbars[stage], parity, wlim)) {
+    // warp-uniform: every lane leaves, or none does (shuffles follow)
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wbars[stage], parity, wlim))) {
       flag_status(p.status, kDevTimeout);
       // let every stage issued and not yet consumed land, this one included
       for (int k = consumed; k < issued; ++k)
