@@ -54,7 +54,7 @@ HBM_REF_GBS = 8000.0
 # DRAM traffic (read + write bytes per launch) of the fused split kernel on
 # this workload, from one ncu capture, and the source hash of the kernel it was
 # taken on; reported only while the kernel is unchanged.
-NCU_TRAFFIC = {"bytes_per_launch": 1073993216 + 2854656, "kernel_sha": "0c72b59777865edf",
+NCU_TRAFFIC = {"bytes_per_launch": 1073992704 + 2834944, "kernel_sha": "b10f3f3fb27d3bd1",
                "profile": "profiles/decode_split_fused_332M.md"}
 
 
