@@ -315,11 +315,32 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
           }
         }
       }
-      const bool ok = active && row < n;
+      if constexpr ((C & (C - 1)) == 0) {
+        const bool ok = active && row < n;
 #pragma unroll
-      for (int hq = 0; hq < G; ++hq) {
-        const float v = group_sum<C>(acc[hq], lane);
-        s[j][hq] = ok ? v : -FLT_MAX;
+        for (int hq = 0; hq < G; ++hq) {
+          const float v = group_sum<C>(acc[hq], lane);
+          s[j][hq] = ok ? v : -FLT_MAX;
+        }
+      } else {
+#pragma unroll
+        for (int hq = 0; hq < G; ++hq) s[j][hq] = acc[hq];
+      }
+    }
+    if constexpr ((C & (C - 1)) != 0) {
+      // Rows of 5 or 6 lanes (D = 80, 96) are summed by a five-level shuffle
+      // chain and a broadcast: all steps' sums at once, as independent
+      // chains whose latencies overlap (at D = 80, 4B-shaped calls: 635 ->
+      // 590 us fused, 426 -> 346 us lite; no gain for the two-level sums of
+      // 4 or 8 lanes)
+#pragma unroll
+      for (int j = 0; j < STEPS; ++j) {
+        const bool ok = active && j * R + g < n;
+#pragma unroll
+        for (int hq = 0; hq < G; ++hq) {
+          const float v = group_sum<C>(s[j][hq], lane);
+          s[j][hq] = ok ? v : -FLT_MAX;
+        }
       }
     }
 
