@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(PrefillPlan<D, NSRC, G>::THREADS, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.x;
-  const int mt = (int)gridDim.y - 1 - (int)blockIdx.y;   // longest tiles first
+  int unit, mt;
+  prefill_cta_tile(unit, mt);   // longest query tiles first
   const int b = unit / p.H_kv, kh = unit % p.H_kv;
   const int m0 = mt * BM;              // first query row of the tile (within the chunk)
   const int S = p.S;                   // query rows

@@ -125,8 +125,8 @@ __global__ void __launch_bounds__(WideCfg<D>::THREADS, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.x;
-  const int mt = (int)gridDim.y - 1 - (int)blockIdx.y;   // longest tiles first
+  int unit, mt;
+  prefill_cta_tile(unit, mt);   // longest query tiles first
   const int H_q = p.H_kv * p.G;
   const int b = unit / p.H_kv, kh = unit % p.H_kv;
   const bool two_heads = p.G == 2;
