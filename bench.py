@@ -590,6 +590,10 @@ def main():
         with ClockSampler(local) as cs:
             q4 = bench_q4_calls(device, stream, peaks, W)
         q4["clocks"] = cs.summary()
+        # the 4B shape (D = 80: a row spans 5 lanes of the 4-bit kernel)
+        with ClockSampler(local) as cs:
+            q4_4b = bench_q4_calls(device, stream, peaks, W, reps=10, w=synth.B4)
+        q4_4b["clocks"] = cs.summary()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -631,6 +635,7 @@ def main():
             line["decode_steps_other_workloads"] = other_decode
         if q4 is not None:
             line["decode_q4_332M"] = q4
+            line["decode_q4_4B"] = q4_4b
         print(json.dumps(line), flush=True)
     if dist_on:
         torch.distributed.destroy_process_group()
@@ -723,11 +728,11 @@ def run_profile_case(args, device):
     sc.close()
 
 
-def bench_q4_calls(device, stream, peaks, W, reps=20):
-    """4-bit caches: one upper-layer decode call per mode of the 332M-shaped
-    workload; GB/s over the 4-bit bytes, and the time against bf16."""
+def bench_q4_calls(device, stream, peaks, W, reps=20, w=None):
+    """4-bit caches: one upper-layer decode call per mode of a workload (the
+    332M-shaped one by default); GB/s over the 4-bit bytes."""
     from cross_layer_kv_gb300 import synth
-    w = synth.M332
+    w = w or synth.M332
     res = {"workload": w.name + " with 4-bit caches (16-channel groups, bf16 scale/min)"}
     for mode in ("vanilla", "lite", "fused"):
         sc = SingleCall("decode", mode, w, device, stream, q4=True)
