@@ -787,6 +787,8 @@ def bench_prefill(device, stream, peaks, W):
     except fkv.FkvError as e:
         res["unavailable"] = str(e)
     ctx.close()
+    if "fused" in res and "vanilla" in res:
+        res["fused_over_vanilla_time"] = res["fused"]["ms"] / res["vanilla"]["ms"]
     return res
 
 
