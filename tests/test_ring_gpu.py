@@ -277,9 +277,10 @@ def test_ring_prefill_before_wrap_and_rejections():
 
 
 # (mode, D, G): the one-source kernel (128-key tiles), the fused kernel for
-# D <= 96 (112-key tiles) and the fused D = 128 kernel (64-key tiles)
-_WRAP_CASES = [("lite", 64, 2), ("vanilla", 80, 1), ("fused", 96, 2), ("fused", 128, 1),
-               ("scaled", 128, 2)]
+# D <= 96 (112-key tiles; G = 1 puts two row tiles of one head in a CTA) and
+# the fused D = 128 kernel (64-key tiles)
+_WRAP_CASES = [("lite", 64, 2), ("vanilla", 80, 1), ("fused", 96, 2), ("fused", 64, 1),
+               ("fused", 128, 1), ("scaled", 128, 2)]
 
 
 @pytest.mark.parametrize("mode,D,G", _WRAP_CASES)
