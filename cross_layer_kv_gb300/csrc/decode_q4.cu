@@ -20,23 +20,31 @@
 namespace fkv {
 namespace {
 
-// Launch shape (FKV_Q4_{WARPS,STAGES,STAGE_BYTES} override it at build time,
-// for tuning sweeps).
-#ifdef FKV_Q4_WARPS
-constexpr int Q4_W = FKV_Q4_WARPS;
+// Launch shape per source count: warps per CTA, ring stages per warp, bytes
+// per stage.  Two sources (fused) need about 255 registers a thread, so 8
+// warps; one source fits in 168, so 12 warps fit and hide more latency (at
+// 12 x 2 x 9 KB the 332M lite call went 70.5 -> 66.3 us and the 4B one
+// 346 -> 302 us against 8 x 2 x 12 KB).  Larger stages spread the per-tile
+// work (row-max shuffles, refill, barrier) over more rows.
+// FKV_Q4_{WARPS,STAGES,STAGE_BYTES}{1,2} override them at build time (sweeps).
+template <int NSRC>
+struct Q4Shape;
+template <>
+struct Q4Shape<1> {
+#ifdef FKV_Q4_WARPS1
+  static constexpr int W = FKV_Q4_WARPS1, NS = FKV_Q4_STAGES1, SB = FKV_Q4_STAGE_BYTES1;
 #else
-constexpr int Q4_W = 8;            // warps per CTA
+  static constexpr int W = 12, NS = 2, SB = 9216;
 #endif
-#ifdef FKV_Q4_STAGES
-constexpr int Q4_NS = FKV_Q4_STAGES;
+};
+template <>
+struct Q4Shape<2> {
+#ifdef FKV_Q4_WARPS2
+  static constexpr int W = FKV_Q4_WARPS2, NS = FKV_Q4_STAGES2, SB = FKV_Q4_STAGE_BYTES2;
 #else
-constexpr int Q4_NS = 2;           // ring stages per warp
+  static constexpr int W = 8, NS = 2, SB = 12288;
 #endif
-#ifdef FKV_Q4_STAGE_BYTES
-constexpr int Q4_SB = FKV_Q4_STAGE_BYTES;
-#else
-constexpr int Q4_SB = 12288;       // bytes per stage (larger tiles spread the per-tile work)
-#endif
+};
 
 template <int D, int NSRC>
 struct Q4Cfg {
@@ -44,7 +52,7 @@ struct Q4Cfg {
   static constexpr int C = D / kQ4Group;              // lanes per row
   static constexpr int R = 32 / C;                    // rows per warp step
   static constexpr int E = kQ4Group;                  // channels per lane
-  static constexpr int STEPS_RAW = Q4_SB / (2 * NSRC * R * ROWB);
+  static constexpr int STEPS_RAW = Q4Shape<NSRC>::SB / (2 * NSRC * R * ROWB);
   static constexpr int STEPS = STEPS_RAW < 1 ? 1 : STEPS_RAW;
   static constexpr int TR = R * STEPS;
   static constexpr int TILE_BYTES = TR * ROWB;
@@ -76,11 +84,11 @@ __device__ __forceinline__ void q4_params(uint32_t w, float& scale, float& lo) {
 }
 
 template <int D, int NSRC, bool WGT, int G>
-__global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitParams p) {
+__global__ void __launch_bounds__(Q4Shape<NSRC>::W * 32, 1) decode_q4_kernel(const SplitParams p) {
   using Cfg = Q4Cfg<D, NSRC>;
   constexpr int C = Cfg::C, R = Cfg::R, E = Cfg::E, TR = Cfg::TR, STEPS = Cfg::STEPS;
   constexpr int ROWB = Cfg::ROWB, TILE = Cfg::TILE_BYTES, STAGE = Cfg::STAGE_BYTES;
-  constexpr int NS = Q4_NS, W = Q4_W;
+  constexpr int NS = Q4Shape<NSRC>::NS, W = Q4Shape<NSRC>::W;
   constexpr int PS = partial_stride(D);
 
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -480,7 +488,8 @@ __global__ void __launch_bounds__(Q4_W * 32, 1) decode_q4_kernel(const SplitPara
 
 template <int D, int NSRC>
 size_t q4_smem_bytes(int B) {
-  return (size_t)Q4_W * Q4_NS * Q4Cfg<D, NSRC>::STAGE_BYTES + decode_aux_bytes(Q4_W, Q4_NS, B);
+  using S = Q4Shape<NSRC>;
+  return (size_t)S::W * S::NS * Q4Cfg<D, NSRC>::STAGE_BYTES + decode_aux_bytes(S::W, S::NS, B);
 }
 
 template <int D, int NSRC, bool WGT, int G>
@@ -513,7 +522,7 @@ cudaError_t launch_q4(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t 
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem_bytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(plan.ctas), dim3(Q4_W * 32), plan.smem_bytes, stream, sp);
+  return launch_pdl(kern, dim3(plan.ctas), dim3(Q4Shape<NSRC>::W * 32), plan.smem_bytes, stream, sp);
 }
 
 template <int D, int NSRC, bool WGT>
@@ -545,14 +554,15 @@ cudaError_t decode_q4_plan(const DecodeArgs& a, int num_sms, DecodePlan* plan) {
   }
   const long long rows = (long long)a.batch * a.kv_heads * a.max_seq;
   long long ctas = a.num_ctas > 0 ? a.num_ctas : num_sms;
-  const long long by_rows = (rows + 64LL * Q4_W - 1) / (64LL * Q4_W);
+  const int W = a.nsrc == 2 ? Q4Shape<2>::W : Q4Shape<1>::W;
+  const long long by_rows = (rows + 64LL * W - 1) / (64LL * W);
   if (a.num_ctas <= 0) ctas = ctas < by_rows ? ctas : by_rows;
   if (ctas < 1) ctas = 1;
   plan->ctas = (int)ctas;
-  plan->warps_per_cta = Q4_W;
+  plan->warps_per_cta = W;
   plan->smem_bytes = smem;
   const size_t units = (size_t)a.batch * a.kv_heads;
-  const size_t slots = (size_t)ctas * Q4_W + units;
+  const size_t slots = (size_t)ctas * W + units;
   plan->partial_bytes = (slots * a.group * partial_stride(a.head_dim) * sizeof(float) + 15) / 16 * 16;
   plan->workspace_bytes = plan->partial_bytes + units * sizeof(unsigned long long);
   return cudaSuccess;
